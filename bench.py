@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of the shared-input batched linear on GB300.
+
+Headline workload (one "step"): the single-token decode batches of a decoder
+layer with bf16 weights -- the q/k/v batch (n_in 4096 -> 4096 + 1024 + 1024)
+then the gate+up batch (n_in 4096 -> 12288 + 12288), t = 1, each one
+``il_matmul_batch`` call over one shared x.  ``value`` is weight GB/s summed
+over ranks (weight bytes as ``WeightRef::bytes`` counts them, divided by the
+device time of the timed steps).  The weights rotate over several resident
+copies so each step streams them from HBM, not L2.
+
+The same JSON line carries every other workload (quantised decode, prefill,
+vocab projection, tiny) as ``per_config`` entries, the roofline of the
+dominant kernel, the end-to-end figure through host buffers, the clocks seen
+during the timed region and the CPU oracle timed on the host as a baseline.
+
+``--impl reference`` times the CPU oracle alone on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+NOMINAL_HBM_GBS = 8000.0
+HEADLINE = wl.DECODE_BF16
+METRIC = "weight GB/s and TFLOP/s per job batch (1 GB300) as % of HBM/tensor roofline"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-per-config", action="store_true", help="headline only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p["bf16_tflops_sustained"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.marks: list[tuple[float, float]] = []
+        self.t_lines: list[float] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._reader, daemon=True).start()
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+            self.t_lines.append(time.time())
+
+    def mark(self, t0: float, t1: float):
+        self.marks.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in zip(self.t_lines, self.lines):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            inside = any(a - 0.06 <= t <= b + 0.06 for a, b in self.marks)
+            rows.append((inside, parts))
+        sel = [p for inside, p in rows if inside] or [p for _, p in rows]
+        if not sel:
+            return None
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in sel if num(p[1]) is not None]
+        mx = [num(p[2]) for p in sel if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in sel:
+            for name, v in zip(names, p[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sel)}
+
+
+# ---------------------------------------------------------------------------
+# timed execution of a list of batches through the C ABI, as one CUDA graph
+# ---------------------------------------------------------------------------
+class Batch:
+    """One uploaded batch: weights (several resident copies), x, y."""
+
+    def __init__(self, sil, torch, inputs: wl.BatchInputs, copies: int):
+        self.inputs = inputs
+        self.t, self.n_in = inputs.t, inputs.n_in
+        self.copies = [[sil.upload_weight(f, buf, n, inputs.n_in) for f, buf, n in inputs.jobs]
+                       for _ in range(copies)]
+        self.x = torch.from_numpy(inputs.x).cuda()
+        self.ys = [torch.empty((inputs.t, n), device="cuda") for _, _, n in inputs.jobs]
+        self.weight_bytes = inputs.weight_bytes
+        self.flops = inputs.flops
+        self.io_bytes = 4 * inputs.t * inputs.n_in + sum(4 * inputs.t * n for _, _, n in inputs.jobs)
+
+    def launch(self, sil, copy: int, stream):
+        sil.matmul_batch(self.x, list(zip(self.copies[copy % len(self.copies)], self.ys)),
+                         stream=stream)
+
+    def free(self):
+        for c in self.copies:
+            for w in c:
+                w.free()
+
+
+def _graph_event(torch):
+    # an event recorded inside a captured graph must be an "external" record node
+    return torch.cuda.Event(enable_timing=True, external=True)
+
+
+def graph_of(torch, sil, batches, steps: int, stream, copy0: int = 0):
+    """Capture `steps` steps (each: every batch once) with an external event after each batch."""
+    events = [_graph_event(torch) for _ in range(steps * len(batches) + 1)]
+    g = torch.cuda.CUDAGraph()
+    launches0 = sil.get_stats()["launches"]
+    with torch.cuda.graph(g, stream=stream):
+        events[0].record(stream)
+        k = 1
+        for s in range(steps):
+            for b in batches:
+                b.launch(sil, copy0 + s, stream)
+                events[k].record(stream)
+                k += 1
+    launches = sil.get_stats()["launches"] - launches0
+    return g, events, launches
+
+
+def per_batch_us(events, n_batches, steps):
+    out = [[] for _ in range(n_batches)]
+    k = 0
+    for _ in range(steps):
+        for j in range(n_batches):
+            out[j].append(events[k].elapsed_time(events[k + 1]) * 1e3)
+            k += 1
+    return [statistics.mean(v) for v in out]
+
+
+def copies_for(batch_bytes: int) -> int:
+    # enough copies that a weight set is re-read only after >= ~1 GB of other weights
+    return max(2, min(8, math.ceil(1.0e9 / max(batch_bytes, 1)) + 1))
+
+
+def run_headline(sil, torch, args, dist, clocks: ClockSampler):
+    stream = torch.cuda.Stream()
+    inputs = [wl.make_workload_batch(HEADLINE, bt, 1, "bf16") for bt in HEADLINE.batches]
+    step_bytes = sum(b.weight_bytes for b in inputs)
+    copies = copies_for(step_bytes)
+    batches = [Batch(sil, torch, b, copies) for b in inputs]
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for s in range(max(3, args.warmup)):
+            for b in batches:
+                b.launch(sil, s, stream)
+    torch.cuda.synchronize()
+
+    # graph of L steps (L divides K), replayed K/L times
+    K = args.steps
+    L = max(d for d in range(1, min(K, 200) + 1) if K % d == 0)
+    g, events, launches_per_graph = graph_of(torch, sil, batches, L, stream)
+    reps = K // L
+    g.replay()  # upload + warm
+    torch.cuda.synchronize()
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for _ in range(reps):
+        g.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    clocks.mark(t0, t1)
+    elapsed_ms = start.elapsed_time(end)
+    ms_local = elapsed_ms / K
+    kern_us = per_batch_us(events, len(batches), L)
+
+    # e2e: host buffers, pinned, copies inside the timed region every step
+    e2e = run_e2e(sil, torch, batches, args, stream)
+    for b in batches:
+        b.free()
+    return {"ms_per_step": ms_local, "step_bytes": step_bytes,
+            "step_flops": sum(b.flops for b in inputs),
+            "kernel_us": kern_us, "batch_names": [bt.name for bt in HEADLINE.batches],
+            "alg_bytes": [b.weight_bytes + b.io_bytes for b in batches],
+            "launches": launches_per_graph * reps, "copies": copies, "e2e": e2e,
+            "graph_steps": L}
+
+
+def run_e2e(sil, torch, batches, args, stream):
+    xs_host = [torch.from_numpy(b.inputs.x).pin_memory() for b in batches]
+    ys_host = [[torch.empty(y.shape, pin_memory=True) for y in b.ys] for b in batches]
+    h2d = sum(x.numel() * 4 for x in xs_host)
+    d2h = sum(y.numel() * 4 for ys in ys_host for y in ys)
+    steps = min(args.steps, 2000)
+
+    def step(s):
+        with torch.cuda.stream(stream):
+            for b, xh in zip(batches, xs_host):
+                b.x.copy_(xh, non_blocking=True)
+            for b in batches:
+                b.launch(sil, s, stream)
+            for b, yh in zip(batches, ys_host):
+                for y, h in zip(b.ys, yh):
+                    h.copy_(y, non_blocking=True)
+        stream.synchronize()
+
+    for s in range(max(3, args.warmup)):
+        step(s)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(steps):
+        step(s)
+    dt = (time.perf_counter() - t0) / steps
+    step_bytes = sum(b.weight_bytes for b in batches)
+    return {"value": step_bytes / dt / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3, "steps": steps}
+
+
+def run_per_config(sil, torch, pk):
+    """Every workload x batch x t x format, one batch per measurement."""
+    out = []
+    stream = torch.cuda.Stream()
+    cache = {}
+    for w in wl.WORKLOADS:
+        for bt in w.batches:
+            for fmt in w.fmts:
+                for t in w.ts:
+                    # timing only: the weight draw is reused across t (fresh x per t)
+                    key = (w.name, bt.name, fmt)
+                    if key not in cache:
+                        cache.clear()
+                        cache[key] = wl.make_workload_batch(w, bt, t, fmt)
+                    base = cache[key]
+                    inp = wl.BatchInputs(fmt, t, bt.n_in, wl.make_x(t, bt.n_in, seed=0), base.jobs)
+                    copies = copies_for(inp.weight_bytes)
+                    b = Batch(sil, torch, inp, copies)
+                    with torch.cuda.stream(stream):
+                        for s in range(3):
+                            b.launch(sil, s, stream)
+                    torch.cuda.synchronize()
+                    iters = max(copies, 8) if t <= 8 else max(2, min(copies, 4))
+                    g, events, _ = graph_of(torch, sil, [b], iters, stream)
+                    g.replay()
+                    torch.cuda.synchronize()
+                    g.replay()
+                    torch.cuda.synchronize()
+                    us = per_batch_us(events, 1, iters)[0]
+                    gbs = inp.weight_bytes / (us * 1e-6) / 1e9
+                    tfl = inp.flops / (us * 1e-6) / 1e12
+                    e = {"workload": w.name, "batch": bt.name, "fmt": fmt, "t": t,
+                         "n_in": bt.n_in, "n_outs": list(bt.n_outs), "us": round(us, 3),
+                         "weight_gbs": round(gbs, 1), "tflops": round(tfl, 3),
+                         "weight_bytes": inp.weight_bytes}
+                    if t <= 8:
+                        e["bound"] = "hbm"
+                        e["frac_hbm_measured"] = round(gbs / pk["hbm_gbs"], 4)
+                        e["frac_hbm_nominal"] = round(gbs / NOMINAL_HBM_GBS, 4)
+                    else:
+                        e["bound"] = "tensor"
+                        e["frac_tensor_burst"] = round(tfl / pk["bf16_tflops"], 4)
+                        e["frac_tensor_sustained"] = round(tfl / pk["bf16_tflops_sustained"], 4)
+                    out.append(e)
+                    del g
+                    b.free()
+                    torch.cuda.synchronize()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on the host (baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_steps(seconds: float, min_steps: int = 1, max_steps: int | None = None):
+    import oracle
+    inputs = [wl.make_workload_batch(HEADLINE, bt, 1, "bf16") for bt in HEADLINE.batches]
+    step_bytes = sum(b.weight_bytes for b in inputs)
+    oracle.matmul_batch(inputs[0].x, inputs[0].jobs[:1])  # load + warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        for b in inputs:
+            oracle.matmul_batch(b.x, b.jobs)
+        n += 1
+        el = time.perf_counter() - t0
+        if (max_steps is not None and n >= max_steps) or (max_steps is None and n >= min_steps
+                                                          and el >= seconds):
+            break
+    return {"value": step_bytes / (el / n) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} full decode steps (q/k/v + gate/up batches, t=1, bf16 weights, "
+                      f"{step_bytes} weight bytes each), single-threaded C, f64 accumulate",
+            "ms_per_step": el / n * 1e3, "steps": n}
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    config = {"workload": "decode_bf16 q/k/v + gate/up batches, t=1, n_in=4096 "
+                          "(n_out 4096+1024+1024 and 12288+12288)",
+              "t": 1, "n_in": 4096, "formats": "bf16"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        steps = max(1, args.steps) if args.steps <= 50 else 20
+        warm = min(args.warmup, 2)
+        if warm:
+            oracle_steps(0, max_steps=warm)
+        r = oracle_steps(0, max_steps=steps)
+        line = {"impl": "reference", "metric": METRIC, "value": round(r["value"], 3),
+                "unit": "GB/s", "n_gpus": args.gpus, "steps": r["steps"], "warmup": warm,
+                "ms_per_step": round(r["ms_per_step"], 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config,
+                "cpu_baseline": {"value": round(r["value"], 3), "unit": "GB/s", "cores": 1,
+                                 "kind": "oracle", "sample": r["sample"]},
+                "e2e": {"value": round(r["value"], 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import torch
+    import shared_input_linear_gb300 as sil
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+        dist = tdist
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    sil.build()
+    sil.load()
+    pk = peaks()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    head = run_headline(sil, torch, args, dist, clocks)
+    clk = clocks.stop()
+
+    ms = head["ms_per_step"]
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = head["step_bytes"] * world / (ms * 1e-3) / 1e9
+
+    per_config = None
+    if rank == 0 and world == 1 and not args.no_per_config:
+        per_config = run_per_config(sil, torch, pk)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = oracle_steps(args.cpu_seconds)
+        cpu = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()
+               if k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        kus = head["kernel_us"]
+        alg = head["alg_bytes"]
+        achieved = sum(alg) / (sum(kus) * 1e-6) / 1e9
+        prof = read_profile_traffic()
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": prof, "peak_source": pk["source"] + " (MEASURED_PEAKS hbm_gbs, burst)",
+                "kernel": "decode_kernel<bf16> (one launch per batch)",
+                "per_launch_us": {n: round(u, 3) for n, u in zip(head["batch_names"], kus)},
+                "alg_bytes_per_launch": dict(zip(head["batch_names"], alg)),
+                "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)}
+        e2e = head["e2e"]
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded N(0,1) x, N(0,0.02) W)",
+                "config": dict(config, parallelism=f"replicas{world}" if world > 1 else "single",
+                               l2=f"weights rotate over {head['copies']} resident copies "
+                                  f"({head['copies'] * head['step_bytes'] / 1e9:.2f} GB > L2)",
+                               timing=f"CUDA graph of {head['graph_steps']} steps replayed, "
+                                      "CUDA events on the launching stream"),
+                "tflops": round(head["step_flops"] * world / (ms * 1e-3) / 1e12, 4),
+                "roofline": roof, "e2e": {k: (round(v, 3) if isinstance(v, float) else v)
+                                          for k, v in e2e.items()},
+                "gpu_launches": head["launches"], "clocks": clk, "cpu_baseline": cpu,
+                "per_config": per_config}
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def read_profile_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel build."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "decode_bf16_qkv_gateup_t1.md")
+    src = os.path.join(ROOT, "shared_input_linear_gb300", "csrc", "gemv.cu")
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+gemv_sha256_16:\s*([0-9a-f]+)", text)
+    if m is None or m.group(2) != digest:
+        return None
+    return float(m.group(1))
+
+
+if __name__ == "__main__":
+    sys.exit(main())

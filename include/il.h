@@ -1,0 +1,161 @@
+/*
+ * il.h -- C ABI of the shared-input batched linear for GB300 (sm_103a).
+ *
+ * One call runs several matmul jobs over one shared fp32 activation:
+ *     y_j[t][n_out_j] = x[t][n_in] * W_j^T        (W_j stored [n_out_j][n_in])
+ * following the accelerator backend contract of oxinfer 0.0.0, src/gpu.rs:
+ * struct `Job` (one matmul of a batch sharing x), `Backend::upload` (prepare
+ * device state for one weight) and `Backend::matmul` (all jobs of a batch in
+ * one submission).  There is no CPU fallback: an error returns a negative
+ * status and launches nothing.
+ *
+ * Weight storage formats (enum `WeightRef` of the same page; the page names
+ * Q8 and Q4 without defining them, this library fixes them as follows):
+ *   IL_BF16: u16 bit patterns of bf16, host layout u16 w[n_out][n_in].
+ *   IL_Q8  : symmetric int8, one fp32 scale per 32-element block along n_in;
+ *            host layout i8 q[n_out][n_in], then f32 d[n_out][n_in/32]
+ *            starting at byte n_out*n_in.  w = fp32(d*q).
+ *   IL_Q4  : symmetric signed 4-bit (two's complement), two per byte, element
+ *            2k in bits 0-3 of byte k and 2k+1 in bits 4-7; one fp32 scale
+ *            per 32-block; host layout u8 p[n_out][n_in/2], then
+ *            f32 d[n_out][n_in/32] starting at byte n_out*n_in/2.
+ *
+ * Threading: every entry point is thread-safe.  The library works on the
+ * CUDA device that is current on the calling thread.
+ */
+#ifndef IL_H_
+#define IL_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define IL_VERSION 1
+
+/* Storage format of a weight (oxinfer src/gpu.rs, enum WeightRef). */
+typedef enum { IL_BF16 = 0, IL_Q8 = 1, IL_Q4 = 2 } il_format;
+
+/* Status codes.  IL_OK is 0; every error is negative.  An entry point that
+ * returns an error has launched no work and written no output. */
+typedef enum {
+  IL_OK = 0,
+  IL_ERR_ARG = -1,            /* null pointer, negative size, misaligned or overlapping buffer */
+  IL_ERR_SHAPE = -2,          /* n_in / n_out inconsistent with a handle, or not a legal size */
+  IL_ERR_FORMAT = -3,         /* unknown storage format */
+  IL_ERR_HANDLE = -4,         /* freed, forged or other-device weight handle */
+  IL_ERR_OOM = -5,            /* device allocation failed */
+  IL_ERR_CUDA = -6,           /* CUDA runtime or launch error */
+  IL_ERR_DEVICE_TIMEOUT = -7, /* a device-side wait gave up (see il_check_device_status) */
+  IL_ERR_UNSUPPORTED = -8     /* no sm_103a device current, or a size beyond a documented limit */
+} il_status;
+
+/* Opaque device weight (the page's `DeviceWeight`).  Owned by the caller,
+ * released with il_free_weight. */
+typedef struct il_weight il_weight;
+
+/* One job of a batch (the page's `Job`): y[t][n_out] = x[t][n_in] * W^T.
+ *   w     : handle from il_upload_weight; its n_in must equal the batch n_in.
+ *   n_out : must equal the handle's n_out.
+ *   y     : DEVICE pointer, fp32 [t][n_out] row-major, 4-byte aligned; it is
+ *           overwritten (not accumulated) and must not overlap x or any other
+ *           job's y. */
+typedef struct {
+  const il_weight* w;
+  int64_t n_out;
+  float* y;
+} il_job;
+
+/* Cumulative counters (the page's `Backend::stats`, as numbers). */
+typedef struct {
+  uint64_t uploads;           /* successful il_upload_weight calls        */
+  uint64_t upload_bytes;      /* host bytes uploaded (WeightRef::bytes)   */
+  uint64_t batches;           /* successful il_matmul_batch calls         */
+  uint64_t jobs;              /* jobs in those batches                    */
+  uint64_t launches;          /* kernels launched by those batches        */
+  uint64_t weight_bytes;      /* weight bytes those batches streamed      */
+  uint64_t flops;             /* 2 * t * n_in * n_out summed over jobs    */
+  uint64_t errors;            /* calls that returned an error             */
+} il_stats;
+
+/*
+ * il_upload_weight -- oxinfer src/gpu.rs, `Backend::upload` ("prepares
+ * device-side state for a weight matrix").
+ *   format   : il_format.
+ *   host_ptr : HOST pointer to the weight in the host layout above; only read
+ *              during the call (it is copied, then repacked on the device).
+ *              Q8/Q4 scales are read with 4-byte loads from the host copy, so
+ *              any alignment is accepted.
+ *   n_out    : rows, 1 <= n_out <= 2^31 - 1.
+ *   n_in     : columns, 1 <= n_in <= 32768; a multiple of 8 for IL_BF16 and of
+ *              32 for IL_Q8 / IL_Q4.
+ * Returns a new handle, or NULL on error (il_last_error() says why).
+ * Synchronous: when it returns the packed weight is resident in HBM.
+ */
+il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int64_t n_in);
+
+/*
+ * il_matmul_batch -- oxinfer src/gpu.rs, `Backend::matmul` ("runs a batch of
+ * matmuls over one shared input in a single submission").
+ *   x      : DEVICE pointer, fp32 [t][n_in] row-major, 16-byte aligned.
+ *   t      : tokens, 0 <= t <= 2^20.  t == 0 is a successful no-op.
+ *   n_in   : must equal every job's handle n_in.
+ *   jobs   : HOST array of n_jobs il_job (read during the call only).
+ *   n_jobs : 0 <= n_jobs <= 4096; 0 is a successful no-op.
+ *   stream : cudaStream_t to enqueue on (NULL = legacy default stream).
+ * All arguments are validated before anything is launched; on any error the
+ * call returns a negative il_status with no work enqueued.  On success the
+ * work is enqueued asynchronously on `stream`; x, y and the handles must stay
+ * valid until it completes.  Tokens t <= 8 run the grouped decode kernel
+ * (each weight byte streamed once); larger t cast x to bf16 once and run the
+ * tensor-core kernel.  Jobs of different formats in one batch are allowed.
+ */
+int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
+                    void* stream);
+
+/* Releases a handle and its device memory (synchronises the device).
+ * NULL is ignored; an unknown pointer is ignored and counted as an error. */
+void il_free_weight(il_weight* w);
+
+/* Host-layout byte size of the weight, oxinfer src/gpu.rs `WeightRef::bytes`:
+ * 2*n_out*n_in (bf16), n_out*n_in*9/8 (Q8), n_out*n_in*5/8 (Q4).  -1 for an
+ * invalid handle. */
+int64_t il_weight_bytes(const il_weight* w);
+
+/* Format and shape of a handle.  Any out pointer may be NULL. */
+int il_weight_info(const il_weight* w, int* format, int64_t* n_out, int64_t* n_in);
+
+/*
+ * il_dequantize_weight -- test hook: writes every element of the uploaded
+ * weight as fp32 to dev_out [n_out][n_in] (DEVICE pointer, 4-byte aligned),
+ * reading the packed device layout with the same element decoders the matmul
+ * kernels use.  bf16 widens exactly; Q8/Q4 give fp32(d*q).  Asynchronous on
+ * `stream`.
+ */
+int il_dequantize_weight(const il_weight* w, float* dev_out, void* stream);
+
+/* Reads (and clears) the device-side status word that bounded waits in the
+ * kernels set when they give up.  Synchronises `stream`.  Returns IL_OK, or
+ * IL_ERR_DEVICE_TIMEOUT if a wait timed out since the last call. */
+int il_check_device_status(void* stream);
+
+/* Message of the last error on this thread ("" if none). */
+const char* il_last_error(void);
+
+/* il_status of the last error on this thread (IL_OK if none); useful after
+ * il_upload_weight returned NULL.  Each entry point clears it on entry. */
+int il_last_status(void);
+
+/* Copies the cumulative counters into *out. */
+int il_get_stats(il_stats* out);
+void il_reset_stats(void);
+
+/* IL_VERSION of the loaded library. */
+int il_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IL_H_ */

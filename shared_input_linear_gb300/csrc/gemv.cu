@@ -1,0 +1,399 @@
+// gemv.cu -- grouped decode kernel for small token counts (t <= 8).
+//
+// Computes, for every job j of a batch over one shared x (oxinfer src/gpu.rs,
+// struct `Job` and `Backend::matmul`):   y_j[t][o] = sum_i x[t][i] * w_j[o][i].
+//
+// Design (GB300):
+//  * One launch covers every job: rows of all jobs are cut into groups of 8
+//    and the groups are concatenated; a row block is 8 warps x G groups.
+//  * Each weight byte is streamed from HBM exactly once, as 16-byte loads per
+//    lane, prefetched P chunks ahead in registers.
+//  * The per-(row, token) dot products run on the tensor cores with
+//    mma.m16n8k16 (bf16 in, fp32 accumulate): the weight is the 16x8 "B"
+//    operand (8 rows), and the "A" operand holds 8 tokens of x split into a
+//    bf16 high part (rows 0-7) and the bf16 rounding of the remainder (rows
+//    8-15), so x keeps ~16 significant bits and one MMA serves any t <= 8.
+//    Q8 / Q4 weights are turned into exact bf16 integers in registers; the
+//    fp32 scale of each 32-block multiplies the fp32 partial of that block.
+//  * x is staged once per CTA in shared memory, already in MMA fragment
+//    order.  When x's K range is large or the batch has few rows, K is split
+//    over the CTAs of a thread-block cluster, whose partial sums are reduced
+//    through distributed shared memory in a fixed rank order (deterministic).
+//  * CTAs are persistent: a cluster walks row blocks with a stride of the
+//    number of clusters, and the prefetch runs across row-block boundaries.
+#include <cooperative_groups.h>
+
+#include <mutex>
+#include <map>
+#include <tuple>
+
+#include "il_internal.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace il {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxSliceK = 4096;  // columns of x staged per CTA (32 bytes each)
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+// (hi pair, lo pair) of two fp32 values: hi = bf16_rn(v), lo = bf16_rn(v - hi).
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+template <int FMT>
+struct Fmt {
+  static constexpr int CK = chunk_k(FMT);       // columns per chunk
+  static constexpr int SPC = CK / 16;           // MMA slots per chunk
+  static constexpr int SV = FMT == IL_BF16 ? 0 : (FMT == IL_Q8 ? 1 : 2);  // uint4 of scales
+};
+
+__device__ __forceinline__ int find_job(const DecodeParams& p, int gidx) {
+  int j = p.n_jobs - 1;
+  while (j > 0 && p.jobs[j].group_begin > gidx) --j;
+  return j;
+}
+
+template <int FMT, int G, int P, bool CLUSTER>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
+  using F = Fmt<FMT>;
+  constexpr int GPB = kWarps * G;
+  constexpr int SVN = F::SV > 0 ? F::SV : 1;
+  extern __shared__ __align__(16) uint8_t smem[];
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int n = lane >> 2;  // weight row within the group (B operand) and token (A / D rows)
+  const int q = lane & 3;
+
+  int rank = 0, cid = blockIdx.x, nclusters = gridDim.x;
+  if (CLUSTER) {
+    rank = (int)cg::this_cluster().block_rank();
+    cid = blockIdx.x / p.slices;
+    nclusters = gridDim.x / p.slices;
+  }
+  const int c_begin = rank * p.chunks_per_slice;
+  const int c_cnt = min(p.chunks_per_slice, p.n_chunks - c_begin);
+  const int my_rbs = (p.n_rowblocks - cid + nclusters - 1) / nclusters;
+  const int total = my_rbs * c_cnt;
+  const int slots = p.chunks_per_slice * F::SPC;
+  uint4* xf = reinterpret_cast<uint4*>(smem);
+  float* red = reinterpret_cast<float*>(smem + (size_t)slots * 512);
+
+  // ---- load cursor: base pointers of this warp's G groups in the row block being loaded
+  const uint8_t* lw[G];
+  const float* ls[G];
+  auto set_load_rb = [&](int rbi) {
+    const int rb = cid + rbi * nclusters;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int gidx = rb * GPB + warp * G + g;
+      lw[g] = nullptr;
+      ls[g] = nullptr;
+      if (rbi < my_rbs && gidx < p.total_groups) {
+        const DecodeJob& jb = p.jobs[find_job(p, gidx)];
+        const int64_t lg = gidx - jb.group_begin;
+        if (FMT == IL_BF16) {
+          lw[g] = jb.w + ((lg * 8 + n) * jb.row_stride + (int64_t)c_begin * 32 + 8 * q) * 2;
+        } else {
+          lw[g] = jb.w + ((lg * jb.row_stride + c_begin) * 32 + lane) * 16;
+          ls[g] = jb.s + ((lg * jb.row_stride + c_begin) * 4 + q) * (4 * F::SV);
+        }
+      }
+    }
+  };
+  constexpr int kWStep = FMT == IL_BF16 ? 64 : 512;  // bytes per chunk along a lane's stream
+  constexpr int kSStep = 16 * SVN;                   // floats per chunk along a q's scale stream
+
+  uint4 qr[P][G];
+  uint4 sr[P][G][SVN];
+  int l_rbi = 0, l_cc = 0;
+  set_load_rb(0);
+  auto load_next = [&](uint4 (&dq)[G], uint4 (&ds)[G][SVN]) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (lw[g] != nullptr) {
+        dq[g] = __ldg(reinterpret_cast<const uint4*>(lw[g] + (int64_t)l_cc * kWStep));
+        if (F::SV > 0) {
+#pragma unroll
+          for (int v = 0; v < F::SV; ++v)
+            ds[g][v] = __ldg(reinterpret_cast<const uint4*>(ls[g] + (int64_t)l_cc * kSStep) + v);
+        }
+      } else {
+        dq[g] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int v = 0; v < SVN; ++v) ds[g][v] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (++l_cc == c_cnt) {
+      l_cc = 0;
+      set_load_rb(++l_rbi);
+    }
+  };
+
+  // Start the weight stream before staging x so HBM is busy from the first cycle.
+#pragma unroll
+  for (int s = 0; s < P; ++s)
+    if (s < total) load_next(qr[s], sr[s]);
+
+  // ---- stage this CTA's K slice of x in fragment order (hi/lo split)
+  for (int e = threadIdx.x; e < slots * 32; e += kThreads) {
+    const int s = e >> 5, L = e & 31, m = L >> 2, qq = L & 3;
+    int k;
+    if (FMT == IL_BF16)
+      k = 32 * (c_begin + (s >> 1)) + 8 * qq + 4 * (s & 1);
+    else
+      k = F::CK * c_begin + 16 * s + 4 * qq;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (m < p.t && k < p.n_in && s < c_cnt * F::SPC) {
+      const float4 xv = *reinterpret_cast<const float4*>(p.x + (int64_t)m * p.x_row_stride + k);
+      split_pair(xv.x, xv.y, v.x, v.y);
+      split_pair(xv.z, xv.w, v.z, v.w);
+    }
+    xf[e] = v;
+  }
+  __syncthreads();
+
+  float acc[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
+
+  int c_rbi = 0, c_cc = 0;
+  for (int f0 = 0; f0 < total; f0 += P) {
+#pragma unroll
+    for (int s = 0; s < P; ++s) {
+      if (f0 + s < total) {
+        uint4 cq[G];
+        uint4 cs[G][SVN];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          cq[g] = qr[s][g];
+#pragma unroll
+          for (int v = 0; v < SVN; ++v) cs[g][v] = sr[s][g][v];
+        }
+        if (f0 + s + P < total) load_next(qr[s], sr[s]);
+
+        const uint4* xs = xf + (c_cc * F::SPC) * 32 + lane;
+        if (FMT == IL_BF16) {
+          const uint4 a0 = xs[0], a1 = xs[32];
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            mma_bf16(acc[g], a0, cq[g].x, cq[g].y);
+            mma_bf16(acc[g], a1, cq[g].z, cq[g].w);
+          }
+        } else if (FMT == IL_Q8) {
+#pragma unroll
+          for (int bb = 0; bb < 2; ++bb) {
+            const uint4 a0 = xs[(2 * bb) * 32], a1 = xs[(2 * bb + 1) * 32];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const uint32_t w0 = bb == 0 ? cq[g].x : cq[g].z;
+              const uint32_t w1 = bb == 0 ? cq[g].y : cq[g].w;
+              float t4[4] = {0.f, 0.f, 0.f, 0.f};
+              uint32_t b0, b1;
+              q8_word_to_bf16x2(w0, b0, b1);
+              mma_bf16(t4, a0, b0, b1);
+              q8_word_to_bf16x2(w1, b0, b1);
+              mma_bf16(t4, a1, b0, b1);
+              const float d0 = __uint_as_float(bb == 0 ? cs[g][0].x : cs[g][0].y);  // row 2q
+              const float d1 = __uint_as_float(bb == 0 ? cs[g][0].z : cs[g][0].w);  // row 2q+1
+              acc[g][0] = fmaf(d0, t4[0], acc[g][0]);
+              acc[g][2] = fmaf(d0, t4[2], acc[g][2]);
+              acc[g][1] = fmaf(d1, t4[1], acc[g][1]);
+              acc[g][3] = fmaf(d1, t4[3], acc[g][3]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const uint4 a0 = xs[(2 * w) * 32], a1 = xs[(2 * w + 1) * 32];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const uint32_t word = w == 0 ? cq[g].x : (w == 1 ? cq[g].y : (w == 2 ? cq[g].z : cq[g].w));
+              float t4[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_bf16(t4, a0, q4_pair_to_bf16x2(word, 0), q4_pair_to_bf16x2(word, 4));
+              mma_bf16(t4, a1, q4_pair_to_bf16x2(word, 8), q4_pair_to_bf16x2(word, 12));
+              const uint4 s01 = cs[g][0], s23 = cs[g][SVN - 1];
+              const uint32_t d0b = w == 0 ? s01.x : (w == 1 ? s01.y : (w == 2 ? s01.z : s01.w));
+              const uint32_t d1b = w == 0 ? s23.x : (w == 1 ? s23.y : (w == 2 ? s23.z : s23.w));
+              const float d0 = __uint_as_float(d0b), d1 = __uint_as_float(d1b);
+              acc[g][0] = fmaf(d0, t4[0], acc[g][0]);
+              acc[g][2] = fmaf(d0, t4[2], acc[g][2]);
+              acc[g][1] = fmaf(d1, t4[1], acc[g][1]);
+              acc[g][3] = fmaf(d1, t4[3], acc[g][3]);
+            }
+          }
+        }
+
+        if (++c_cc == c_cnt) {  // ---- epilogue of one row block
+          c_cc = 0;
+          const int rb = cid + c_rbi * nclusters;
+          if (!CLUSTER) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const int gidx = rb * GPB + warp * G + g;
+              if (gidx < p.total_groups && n < p.t) {
+                const DecodeJob& jb = p.jobs[find_job(p, gidx)];
+                const int row0 = (gidx - jb.group_begin) * 8 + 2 * q;
+                float* y = jb.y + (int64_t)n * jb.n_out + row0;
+                if (row0 < jb.n_out) y[0] = acc[g][0] + acc[g][2];
+                if (row0 + 1 < jb.n_out) y[1] = acc[g][1] + acc[g][3];
+              }
+              acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
+            }
+          } else {
+            float* rbuf = red + (c_rbi & 1) * GPB * 64;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const int gl = warp * G + g;
+              *reinterpret_cast<float2*>(rbuf + gl * 64 + n * 8 + 2 * q) =
+                  make_float2(acc[g][0] + acc[g][2], acc[g][1] + acc[g][3]);
+              acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
+            }
+            cg::cluster_group cluster = cg::this_cluster();
+            cluster.sync();
+            const int per = (GPB * 64 + p.slices - 1) / p.slices;
+            const int e_end = min(GPB * 64, (rank + 1) * per);
+            for (int e = rank * per + threadIdx.x; e < e_end; e += kThreads) {
+              const int gl = e >> 6, m = (e >> 3) & 7, r = e & 7;
+              const int gidx = rb * GPB + gl;
+              if (gidx < p.total_groups && m < p.t) {
+                float v = 0.f;
+                for (int src = 0; src < p.slices; ++src)
+                  v += cluster.map_shared_rank(rbuf, src)[e];
+                const DecodeJob& jb = p.jobs[find_job(p, gidx)];
+                const int row = (gidx - jb.group_begin) * 8 + r;
+                if (row < jb.n_out) jb.y[(int64_t)m * jb.n_out + row] = v;
+              }
+            }
+          }
+          ++c_rbi;
+        }
+      }
+    }
+  }
+  if (CLUSTER) cg::this_cluster().sync();  // keep shared memory alive for remote readers
+}
+
+// ---------------------------------------------------------------------------
+// host side: plan + launch
+// ---------------------------------------------------------------------------
+// Prefetch depth: chunk loads in flight per warp, split over its G groups.
+template <int FMT>
+struct Tuning;
+template <> struct Tuning<IL_BF16> { static constexpr int kLoads = 8; };
+template <> struct Tuning<IL_Q8> { static constexpr int kLoads = 4; };
+template <> struct Tuning<IL_Q4> { static constexpr int kLoads = 4; };
+
+using KernelFn = void (*)(DecodeParams);
+
+template <int FMT, int G, bool CLUSTER>
+KernelFn kernel_for() {
+  constexpr int P = Tuning<FMT>::kLoads / G > 2 ? Tuning<FMT>::kLoads / G : 2;
+  return decode_kernel<FMT, G, P, CLUSTER>;
+}
+
+KernelFn select(int fmt, int G, bool cluster) {
+#define IL_SEL(F)                                                                      \
+  if (fmt == F) {                                                                      \
+    if (G == 1) return cluster ? kernel_for<F, 1, true>() : kernel_for<F, 1, false>(); \
+    return cluster ? kernel_for<F, 2, true>() : kernel_for<F, 2, false>();             \
+  }
+  IL_SEL(IL_BF16)
+  IL_SEL(IL_Q8)
+  IL_SEL(IL_Q4)
+#undef IL_SEL
+  return nullptr;
+}
+
+std::mutex g_occ_mu;
+std::map<std::tuple<int, int, int, int, int, int>, int> g_occ;  // -> clusters (or CTAs) resident
+
+}  // namespace
+
+cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream, int num_sms,
+                          int* launches) {
+  DecodeParams p = pin;
+  const int ck = chunk_k(fmt);
+  const int spc = ck / 16;
+  // groups / rows
+  const int G = (p.total_groups + 15) / 16 >= num_sms ? 2 : 1;
+  const int gpb = kWarps * G;
+  p.n_rowblocks = (p.total_groups + gpb - 1) / gpb;
+  // K split over a cluster: at least enough slices to keep a slice <= kMaxSliceK
+  // columns; more when there are too few row blocks to cover the SMs twice.
+  const int max_cps = kMaxSliceK / ck;
+  int C = (p.n_chunks + max_cps - 1) / max_cps;
+  while (C < 8 && C < p.n_chunks && p.n_rowblocks * C < 2 * num_sms) ++C;
+  int cps = (p.n_chunks + C - 1) / C;
+  C = (p.n_chunks + cps - 1) / cps;
+  if (C > 8) return cudaErrorInvalidValue;
+  p.slices = C;
+  p.chunks_per_slice = cps;
+  const bool cluster = C > 1;
+  const size_t smem = (size_t)cps * spc * 512 + (cluster ? 2 * gpb * 64 * sizeof(float) : 0);
+
+  KernelFn fn = select(fmt, G, cluster);
+  if (fn == nullptr) return cudaErrorInvalidValue;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  if (cluster) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int resident = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    auto key = std::make_tuple(dev, fmt, G, C, (int)cluster, (int)smem);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) {
+      resident = it->second;
+    } else {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (cluster) {
+        cfg.gridDim = dim3(C * p.n_rowblocks);
+        e = cudaOccupancyMaxActiveClusters(&resident, fn, &cfg);
+      } else {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
+        resident = per_sm * num_sms;
+      }
+      if (e != cudaSuccess) return e;
+      if (resident < 1) return cudaErrorInvalidConfiguration;
+      g_occ[key] = resident;
+    }
+  }
+  const int nclusters = p.n_rowblocks < resident ? p.n_rowblocks : resident;
+  cfg.gridDim = dim3(nclusters * C);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p);
+  if (launches) ++*launches;
+  return e;
+}
+
+}  // namespace il

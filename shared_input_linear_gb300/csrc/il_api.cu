@@ -1,0 +1,451 @@
+// il_api.cu -- the C ABI (include/il.h): handle registry, validation,
+// error reporting, statistics and dispatch to the kernels.
+//
+// Contract followed (oxinfer 0.0.0, src/gpu.rs): `Backend::upload` prepares
+// device state for one weight; `Backend::matmul` runs every job of a batch
+// over one shared x in one submission and, when it cannot, computes nothing.
+// Here "computes nothing" is: every argument is validated before the first
+// launch, and an error returns a negative status with nothing enqueued.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <new>
+#include <string>
+#include <unordered_set>
+#include <utility>
+#include <vector>
+#include <algorithm>
+
+#include "il_internal.cuh"
+
+using namespace il;
+
+namespace {
+
+constexpr int64_t kMaxNIn = 32768;
+constexpr int64_t kMaxNOut = 2147483647;
+constexpr int64_t kMaxT = 1 << 20;
+constexpr int kMaxJobs = 4096;
+
+thread_local std::string t_last_error;
+thread_local int t_last_status = IL_OK;
+
+void clear_error() {
+  t_last_error.clear();
+  t_last_status = IL_OK;
+}
+
+struct Stats {
+  std::atomic<uint64_t> uploads{0}, upload_bytes{0}, batches{0}, jobs{0}, launches{0},
+      weight_bytes{0}, flops{0}, errors{0};
+} g_stats;
+
+std::mutex g_reg_mu;
+std::unordered_set<const PackedWeight*> g_registry;
+
+struct DeviceState {
+  bool ok = false;
+  int num_sms = 0;
+  int major = 0, minor = 0;
+  unsigned* status = nullptr;  // device word set by bounded waits that gave up
+};
+std::mutex g_dev_mu;
+std::map<int, DeviceState> g_devices;
+
+// Scratch for the bf16 copy of x (tensor-core path), one buffer per (device, stream).
+struct Scratch {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_scratch_mu;
+std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  t_last_status = code;
+  g_stats.errors.fetch_add(1);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(IL_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Host-side fault injection for the out-of-memory paths: with
+// IL_FAULT_ALLOC_FAIL_AFTER=k the (k+1)-th device allocation of the process fails.
+std::atomic<long> g_alloc_count{0};
+cudaError_t il_malloc(void** p, size_t bytes) {
+  const char* env = getenv("IL_FAULT_ALLOC_FAIL_AFTER");
+  if (env != nullptr && *env != '\0') {
+    const long limit = strtol(env, nullptr, 10);
+    if (g_alloc_count.fetch_add(1) >= limit) {
+      *p = nullptr;
+      return cudaErrorMemoryAllocation;
+    }
+  }
+  return cudaMalloc(p, bytes);
+}
+
+// Device of the calling thread, checked to be sm_103.
+int current_device(DeviceState** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceState& st = g_devices[dev];
+  if (!st.ok) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    st.major = prop.major;
+    st.minor = prop.minor;
+    st.num_sms = prop.multiProcessorCount;
+    if (!(prop.major == 10 && prop.minor == 3))
+      return fail(IL_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                  dev, prop.major, prop.minor);
+    void* s = nullptr;
+    e = il_malloc(&s, 256);
+    if (e != cudaSuccess) return fail(IL_ERR_OOM, "allocating the device status word failed");
+    e = cudaMemset(s, 0, 256);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+    st.status = static_cast<unsigned*>(s);
+    st.ok = true;
+  }
+  *out = &st;
+  return dev;
+}
+
+bool known_handle(const il_weight* h) {
+  const PackedWeight* w = reinterpret_cast<const PackedWeight*>(h);
+  std::lock_guard<std::mutex> lk(g_reg_mu);
+  return g_registry.count(w) != 0 && w->magic == kWeightMagic;
+}
+
+int64_t host_bytes(int format, int64_t n_out, int64_t n_in) {
+  if (format == IL_BF16) return 2 * n_out * n_in;
+  if (format == IL_Q8) return n_out * n_in + 4 * n_out * (n_in / 32);
+  return n_out * (n_in / 2) + 4 * n_out * (n_in / 32);
+}
+
+int get_scratch(int dev, cudaStream_t stream, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  Scratch& s = g_scratch[{dev, stream}];
+  if (s.bytes < bytes) {
+    if (s.ptr != nullptr) {
+      // The old buffer may still be read by work queued on `stream`.
+      cudaError_t e = cudaStreamSynchronize(stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+      cudaFree(s.ptr);
+      s.ptr = nullptr;
+      s.bytes = 0;
+    }
+    size_t want = bytes + bytes / 4;
+    cudaError_t e = il_malloc(&s.ptr, want);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(IL_ERR_OOM, "allocating %zu bytes of scratch failed", want);
+    }
+    s.bytes = want;
+  }
+  *out = s.ptr;
+  return IL_OK;
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+}  // namespace
+
+extern "C" {
+
+int il_version(void) { return IL_VERSION; }
+
+const char* il_last_error(void) { return t_last_error.c_str(); }
+
+int il_last_status(void) { return t_last_status; }
+
+int il_get_stats(il_stats* out) {
+  if (out == nullptr) return fail(IL_ERR_ARG, "il_get_stats: out is NULL");
+  out->uploads = g_stats.uploads.load();
+  out->upload_bytes = g_stats.upload_bytes.load();
+  out->batches = g_stats.batches.load();
+  out->jobs = g_stats.jobs.load();
+  out->launches = g_stats.launches.load();
+  out->weight_bytes = g_stats.weight_bytes.load();
+  out->flops = g_stats.flops.load();
+  out->errors = g_stats.errors.load();
+  return IL_OK;
+}
+
+void il_reset_stats(void) {
+  g_stats.uploads = 0;
+  g_stats.upload_bytes = 0;
+  g_stats.batches = 0;
+  g_stats.jobs = 0;
+  g_stats.launches = 0;
+  g_stats.weight_bytes = 0;
+  g_stats.flops = 0;
+  g_stats.errors = 0;
+}
+
+il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int64_t n_in) {
+  clear_error();
+  if (format != IL_BF16 && format != IL_Q8 && format != IL_Q4) {
+    fail(IL_ERR_FORMAT, "il_upload_weight: unknown format %d", format);
+    return nullptr;
+  }
+  if (host_ptr == nullptr) {
+    fail(IL_ERR_ARG, "il_upload_weight: host_ptr is NULL");
+    return nullptr;
+  }
+  if (n_out < 1 || n_out > kMaxNOut || n_in < 1 || n_in > kMaxNIn) {
+    fail(IL_ERR_SHAPE, "il_upload_weight: n_out=%lld n_in=%lld out of range", (long long)n_out,
+         (long long)n_in);
+    return nullptr;
+  }
+  if (format == IL_BF16 && n_in % 8 != 0) {
+    fail(IL_ERR_SHAPE, "il_upload_weight: bf16 needs n_in %% 8 == 0 (got %lld)", (long long)n_in);
+    return nullptr;
+  }
+  if (format != IL_BF16 && n_in % 32 != 0) {
+    fail(IL_ERR_SHAPE, "il_upload_weight: Q8/Q4 need n_in %% 32 == 0 (got %lld)", (long long)n_in);
+    return nullptr;
+  }
+  DeviceState* ds = nullptr;
+  const int dev = current_device(&ds);
+  if (dev < 0) return nullptr;
+
+  PackedWeight* w = new (std::nothrow) PackedWeight();
+  if (w == nullptr) {
+    fail(IL_ERR_OOM, "il_upload_weight: host allocation failed");
+    return nullptr;
+  }
+  w->magic = kWeightMagic;
+  w->format = format;
+  w->device = dev;
+  w->n_out = n_out;
+  w->n_in = n_in;
+  w->n_out_pad = (n_out + kGroupRows - 1) / kGroupRows * kGroupRows;
+  w->n_in_pad = (n_in + kPadK - 1) / kPadK * kPadK;
+  w->n_groups = w->n_out_pad / kGroupRows;
+  w->n_chunks = w->n_in_pad / chunk_k(format);
+  w->host_bytes = host_bytes(format, n_out, n_in);
+  size_t qbytes = format == IL_BF16 ? (size_t)w->n_out_pad * w->n_in_pad * 2
+                                    : (size_t)w->n_groups * w->n_chunks * kChunkBytes;
+  size_t sbytes = format == IL_BF16 ? 0 : (size_t)w->n_groups * w->n_chunks * chunk_scale_bytes(format);
+  size_t soff = (qbytes + 255) / 256 * 256;
+  w->device_bytes = soff + sbytes;
+
+  void* mem = nullptr;
+  cudaError_t e = il_malloc(&mem, w->device_bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    const size_t want = w->device_bytes;
+    delete w;
+    fail(IL_ERR_OOM, "il_upload_weight: cudaMalloc(%zu) failed", want);
+    return nullptr;
+  }
+  w->quants = static_cast<uint8_t*>(mem);
+  w->scales = sbytes ? reinterpret_cast<float*>(w->quants + soff) : nullptr;
+
+  void* staging = nullptr;
+  e = il_malloc(&staging, (size_t)w->host_bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(mem);
+    const long long want = (long long)w->host_bytes;
+    delete w;
+    fail(IL_ERR_OOM, "il_upload_weight: staging cudaMalloc(%lld) failed", want);
+    return nullptr;
+  }
+  e = cudaMemcpy(staging, host_ptr, (size_t)w->host_bytes, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = launch_pack(*w, static_cast<const uint8_t*>(staging), 0);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+  cudaFree(staging);
+  if (e != cudaSuccess) {
+    cudaFree(mem);
+    delete w;
+    cuda_fail(e, "il_upload_weight: copy/pack");
+    return nullptr;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_reg_mu);
+    g_registry.insert(w);
+  }
+  g_stats.uploads.fetch_add(1);
+  g_stats.upload_bytes.fetch_add((uint64_t)w->host_bytes);
+  return reinterpret_cast<il_weight*>(w);
+}
+
+void il_free_weight(il_weight* h) {
+  if (h == nullptr) return;
+  PackedWeight* w = reinterpret_cast<PackedWeight*>(h);
+  {
+    std::lock_guard<std::mutex> lk(g_reg_mu);
+    if (g_registry.erase(w) == 0) {
+      fail(IL_ERR_HANDLE, "il_free_weight: unknown handle");
+      return;
+    }
+  }
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != w->device) cudaSetDevice(w->device);
+  cudaFree(w->quants);  // synchronises the device
+  if (prev >= 0 && prev != w->device) cudaSetDevice(prev);
+  w->magic = 0;
+  delete w;
+}
+
+int64_t il_weight_bytes(const il_weight* h) {
+  if (h == nullptr || !known_handle(h)) return -1;
+  return reinterpret_cast<const PackedWeight*>(h)->host_bytes;
+}
+
+int il_weight_info(const il_weight* h, int* format, int64_t* n_out, int64_t* n_in) {
+  if (h == nullptr || !known_handle(h)) return fail(IL_ERR_HANDLE, "il_weight_info: invalid handle");
+  const PackedWeight* w = reinterpret_cast<const PackedWeight*>(h);
+  if (format) *format = w->format;
+  if (n_out) *n_out = w->n_out;
+  if (n_in) *n_in = w->n_in;
+  return IL_OK;
+}
+
+int il_dequantize_weight(const il_weight* h, float* dev_out, void* stream) {
+  clear_error();
+  if (h == nullptr || !known_handle(h)) return fail(IL_ERR_HANDLE, "il_dequantize_weight: invalid handle");
+  if (dev_out == nullptr) return fail(IL_ERR_ARG, "il_dequantize_weight: dev_out is NULL");
+  if (reinterpret_cast<uintptr_t>(dev_out) % 4 != 0)
+    return fail(IL_ERR_ARG, "il_dequantize_weight: dev_out is not 4-byte aligned");
+  const PackedWeight* w = reinterpret_cast<const PackedWeight*>(h);
+  DeviceState* ds = nullptr;
+  const int dev = current_device(&ds);
+  if (dev < 0) return dev;
+  if (dev != w->device) return fail(IL_ERR_HANDLE, "il_dequantize_weight: handle lives on device %d", w->device);
+  cudaError_t e = launch_dequant(*w, dev_out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "il_dequantize_weight: launch");
+  return IL_OK;
+}
+
+int il_check_device_status(void* stream) {
+  DeviceState* ds = nullptr;
+  const int dev = current_device(&ds);
+  if (dev < 0) return dev;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, ds->status, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ds->status, 0, sizeof word, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "il_check_device_status");
+  if (word != 0) return fail(IL_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (code 0x%x)", word);
+  return IL_OK;
+}
+
+int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
+                    void* stream_) {
+  clear_error();
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (t < 0 || t > kMaxT) return fail(IL_ERR_ARG, "il_matmul_batch: t=%lld out of range", (long long)t);
+  if (n_jobs < 0 || n_jobs > kMaxJobs)
+    return fail(IL_ERR_ARG, "il_matmul_batch: n_jobs=%d out of range", n_jobs);
+  if (t == 0 || n_jobs == 0) return IL_OK;
+  if (x == nullptr) return fail(IL_ERR_ARG, "il_matmul_batch: x is NULL");
+  if (jobs == nullptr) return fail(IL_ERR_ARG, "il_matmul_batch: jobs is NULL");
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0)
+    return fail(IL_ERR_ARG, "il_matmul_batch: x is not 16-byte aligned");
+  if (n_in < 1 || n_in > kMaxNIn)
+    return fail(IL_ERR_SHAPE, "il_matmul_batch: n_in=%lld out of range", (long long)n_in);
+
+  DeviceState* ds = nullptr;
+  const int dev = current_device(&ds);
+  if (dev < 0) return dev;
+
+  // ---- validate every job before launching anything
+  std::vector<std::pair<uintptr_t, uintptr_t>> ranges;
+  ranges.reserve(n_jobs + 1);
+  ranges.emplace_back(reinterpret_cast<uintptr_t>(x),
+                      reinterpret_cast<uintptr_t>(x) + (uintptr_t)(t * n_in * 4));
+  uint64_t wbytes = 0, flops = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_reg_mu);
+    for (int j = 0; j < n_jobs; ++j) {
+      const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[j].w);
+      if (w == nullptr || g_registry.count(w) == 0 || w->magic != kWeightMagic)
+        return fail(IL_ERR_HANDLE, "il_matmul_batch: job %d has an invalid weight handle", j);
+      if (w->device != dev)
+        return fail(IL_ERR_HANDLE, "il_matmul_batch: job %d weight lives on device %d, current is %d",
+                    j, w->device, dev);
+      if (w->n_in != n_in)
+        return fail(IL_ERR_SHAPE, "il_matmul_batch: job %d weight n_in=%lld, batch n_in=%lld", j,
+                    (long long)w->n_in, (long long)n_in);
+      if (jobs[j].n_out != w->n_out)
+        return fail(IL_ERR_SHAPE, "il_matmul_batch: job %d n_out=%lld, weight n_out=%lld", j,
+                    (long long)jobs[j].n_out, (long long)w->n_out);
+      if (jobs[j].y == nullptr) return fail(IL_ERR_ARG, "il_matmul_batch: job %d y is NULL", j);
+      if (reinterpret_cast<uintptr_t>(jobs[j].y) % 4 != 0)
+        return fail(IL_ERR_ARG, "il_matmul_batch: job %d y is not 4-byte aligned", j);
+      const uintptr_t y0 = reinterpret_cast<uintptr_t>(jobs[j].y);
+      ranges.emplace_back(y0, y0 + (uintptr_t)(t * w->n_out * 4));
+      wbytes += (uint64_t)w->host_bytes;
+      flops += 2ull * (uint64_t)t * (uint64_t)n_in * (uint64_t)w->n_out;
+    }
+  }
+  std::vector<std::pair<uintptr_t, uintptr_t>> sorted = ranges;
+  std::sort(sorted.begin(), sorted.end());
+  for (size_t i = 1; i < sorted.size(); ++i)
+    if (overlaps(sorted[i - 1].first, sorted[i - 1].second, sorted[i].first, sorted[i].second))
+      return fail(IL_ERR_ARG, "il_matmul_batch: x and the y buffers must not overlap");
+
+  // ---- dispatch (per format; decode kernel for t <= 8 in token groups of 8)
+  int launches = 0;
+  cudaError_t e = cudaSuccess;
+  for (int fmt = IL_BF16; fmt <= IL_Q4 && e == cudaSuccess; ++fmt) {
+    std::vector<int> idx;
+    for (int j = 0; j < n_jobs; ++j)
+      if (reinterpret_cast<const PackedWeight*>(jobs[j].w)->format == fmt) idx.push_back(j);
+    if (idx.empty()) continue;
+    for (size_t j0 = 0; j0 < idx.size() && e == cudaSuccess; j0 += kMaxDecodeJobs) {
+      const size_t j1 = std::min(idx.size(), j0 + (size_t)kMaxDecodeJobs);
+      for (int64_t t0 = 0; t0 < t && e == cudaSuccess; t0 += 8) {
+        DecodeParams p;
+        memset(&p, 0, sizeof p);
+        p.x = x + t0 * n_in;
+        p.t = (int)std::min<int64_t>(8, t - t0);
+        p.x_row_stride = (int)n_in;
+        p.n_in = (int)n_in;
+        int groups = 0;
+        for (size_t j = j0; j < j1; ++j) {
+          const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[idx[j]].w);
+          DecodeJob& dj = p.jobs[p.n_jobs++];
+          dj.w = w->quants;
+          dj.s = w->scales;
+          dj.y = jobs[idx[j]].y + t0 * w->n_out;
+          dj.n_out = (int32_t)w->n_out;
+          dj.group_begin = groups;
+          dj.row_stride = fmt == IL_BF16 ? w->n_in_pad : w->n_chunks;
+          groups += (int)w->n_groups;
+          p.n_chunks = (int)w->n_chunks;
+        }
+        p.total_groups = groups;
+        e = launch_decode(fmt, p, stream, ds->num_sms, &launches);
+      }
+    }
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "il_matmul_batch: launch");
+  g_stats.batches.fetch_add(1);
+  g_stats.jobs.fetch_add((uint64_t)n_jobs);
+  g_stats.launches.fetch_add((uint64_t)launches);
+  g_stats.weight_bytes.fetch_add(wbytes);
+  g_stats.flops.fetch_add(flops);
+  return IL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,135 @@
+// il_internal.cuh -- declarations shared by the translation units of the
+// library: the packed device layout of a weight, the job tables handed to the
+// kernels, the element decoders used by both the matmul kernels and the
+// dequantise hook, and the launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/il.h"
+
+namespace il {
+
+// ---------------------------------------------------------------------------
+// Packed device layout
+// ---------------------------------------------------------------------------
+// Rows are padded to a multiple of 8 (one "row group", the n=8 side of the
+// decode MMA) and columns to a multiple of 128 (one Q4 chunk); padding is 0.
+//
+// BF16: plain row-major u16 [n_out_pad][n_in_pad].  The decode kernel reads
+//   16 bytes (8 consecutive k) per lane; the tensor-core kernel tiles it with
+//   TMA (K-major, 128-byte swizzle).
+// Q8 / Q4: chunk-major.  A chunk is 8 rows x kChunkK columns and is exactly
+//   512 bytes of quants: lane L of a warp owns bytes [16L, 16L+16) of it.
+//   With n = L/4 (row in group) and q = L%4, the 16 bytes hold the elements
+//   the lane feeds to the MMAs of that chunk (see pack.cu for the order).
+//   Scales are a separate chunk-major stream: for each (group, chunk) and each
+//   q = 0..3, the scales of rows 2q and 2q+1 for every 32-block of the chunk.
+constexpr int kGroupRows = 8;
+constexpr int kPadK = 128;
+constexpr int kChunkBytes = 512;
+
+__host__ __device__ constexpr int chunk_k(int fmt) { return fmt == IL_BF16 ? 32 : (fmt == IL_Q8 ? 64 : 128); }
+__host__ __device__ constexpr int blocks_per_chunk(int fmt) { return fmt == IL_Q8 ? 2 : (fmt == IL_Q4 ? 4 : 0); }
+// Scale bytes per (group, chunk): 8 rows x blocks x 4 bytes.
+__host__ __device__ constexpr int chunk_scale_bytes(int fmt) { return 32 * blocks_per_chunk(fmt); }
+
+struct PackedWeight {
+  uint64_t magic;
+  int format;
+  int device;
+  int64_t n_out, n_in;
+  int64_t n_out_pad, n_in_pad;
+  int64_t n_groups, n_chunks;  // n_out_pad / 8, n_in_pad / chunk_k
+  uint8_t* quants;             // device, packed as above
+  float* scales;               // device, Q8/Q4 only
+  int64_t host_bytes;          // WeightRef::bytes
+  size_t device_bytes;
+};
+constexpr uint64_t kWeightMagic = 0x696c5f7765696768ull;  // "il_weigh"
+
+// ---------------------------------------------------------------------------
+// Decode (t <= 8) job table, passed by value as a kernel parameter
+// ---------------------------------------------------------------------------
+constexpr int kMaxDecodeJobs = 32;
+
+struct DecodeJob {
+  const uint8_t* w;      // packed quants / bf16
+  const float* s;        // packed scales (Q8/Q4)
+  float* y;              // [t][n_out]
+  int32_t n_out;
+  int32_t group_begin;   // first global group index of this job
+  int64_t row_stride;    // bf16: n_in_pad (elements); Q: n_chunks (chunks per group)
+};
+
+struct DecodeParams {
+  const float* x;        // [t][n_in] fp32
+  int t;                 // 1..8 tokens handled by this launch
+  int x_row_stride;      // elements between token rows of x
+  int n_in;
+  int n_chunks;          // chunks over n_in_pad
+  int chunks_per_slice;  // chunks per cluster rank (K slice)
+  int slices;            // cluster size along K
+  int total_groups;
+  int n_rowblocks;
+  int n_jobs;
+  DecodeJob jobs[kMaxDecodeJobs];
+};
+
+// ---------------------------------------------------------------------------
+// Element decoders (shared by the decode kernel and the dequantise hook)
+// ---------------------------------------------------------------------------
+// Q8: one 32-bit word holds 4 int8; returns bf16x2 pairs (e0,e1) and (e2,e3),
+// each value exactly q (|q| <= 128 fits bf16's 8 significant bits).  Uses the
+// float with exponent 2^23: its low mantissa byte is an unsigned integer.
+__device__ __forceinline__ void q8_word_to_bf16x2(uint32_t word, uint32_t& lo01, uint32_t& hi23) {
+  const uint32_t u = word ^ 0x80808080u;  // q + 128 as unsigned bytes
+  const float2 m01 = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)));
+  const float2 m23 = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)));
+  const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+  const float2 q01 = __fadd2_rn(m01, bias);
+  const float2 q23 = __fadd2_rn(m23, bias);
+  // q is exact in bf16, so the low 16 bits of each fp32 are zero: keep the high halves.
+  lo01 = __byte_perm(__float_as_uint(q01.x), __float_as_uint(q01.y), 0x7632);
+  hi23 = __byte_perm(__float_as_uint(q23.x), __float_as_uint(q23.y), 0x7632);
+}
+
+// Q4: nibbles at bit s and bit s+16 of `word` -> bf16x2 (low half from bit s).
+// bf16 0x4300 is 128 with a 7-bit integer mantissa; xor 8 maps the two's
+// complement nibble to q+8, and subtracting 136 leaves q exactly.
+__device__ __forceinline__ uint32_t q4_pair_to_bf16x2(uint32_t word, int s) {
+  const uint32_t v = ((word >> s) & 0x000F000Fu) ^ 0x43084308u;
+  __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v);
+  const __nv_bfloat162 bias = __floats2bfloat162_rn(136.0f, 136.0f);
+  b = __hsub2(b, bias);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------------------
+// Launchers (each returns a cudaError_t; the API layer maps it to il_status)
+// ---------------------------------------------------------------------------
+cudaError_t launch_pack(const PackedWeight& w, const uint8_t* staging, cudaStream_t stream);
+cudaError_t launch_dequant(const PackedWeight& w, float* out, cudaStream_t stream);
+cudaError_t launch_decode(int fmt, const DecodeParams& p, cudaStream_t stream, int num_sms,
+                          int* launches);
+cudaError_t launch_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_in_pad,
+                             __nv_bfloat16* out, cudaStream_t stream);
+
+struct GemmJob {
+  const PackedWeight* w;
+  float* y;
+};
+// Tensor-core path for large t (bf16 weights): xb is x cast to bf16,
+// [t][n_in_pad], zero in the padding columns.
+cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad,
+                             const GemmJob* jobs, int n_jobs, cudaStream_t stream, int num_sms,
+                             unsigned* status, int* launches);
+
+}  // namespace il

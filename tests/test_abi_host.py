@@ -1,0 +1,65 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it builds for sm_103a,
+loads, and exports every function ``include/il.h`` declares.  No compute call
+is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "il.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(il_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def libil():
+    import shared_input_linear_gb300 as sil
+    sil.build()
+    return ctypes.CDLL(sil.LIB_PATH)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("il_upload_weight", "il_matmul_batch", "il_free_weight", "il_weight_bytes",
+                 "il_dequantize_weight", "il_last_error", "il_get_stats"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(libil):
+    missing = [n for n in declared_functions() if not hasattr(libil, n)]
+    assert not missing, f"declared in il.h but not exported: {missing}"
+
+
+def test_version_needs_no_device(libil):
+    libil.il_version.restype = ctypes.c_int
+    assert libil.il_version() == 1
+
+
+def test_binding_names_match_abi():
+    import shared_input_linear_gb300 as sil
+    for name in ("upload_weight", "matmul_batch", "free_weight", "weight_bytes",
+                 "dequantize_weight", "get_stats", "last_error", "check_device_status"):
+        assert callable(getattr(sil, name))
+
+
+def test_product_path_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "shared_input_linear_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in src.lower(), f"{f} mentions the oracle"
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import shared_input_linear_gb300 as sil
+    monkeypatch.setattr(sil, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(sil, "_lib", None)
+    with pytest.raises(sil.ILError):
+        sil.load()

@@ -1,0 +1,189 @@
+"""Boundary behaviour of the C ABI on a GPU: every bad call returns its documented
+status, launches nothing and leaves every output untouched (oxinfer src/gpu.rs,
+`Backend::matmul`: an unsuccessful call computes nothing)."""
+import ctypes
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import workloads as wl
+from gpu_util import lib
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def sil():
+    import torch
+    torch.cuda.set_device(0)
+    return lib()
+
+
+@pytest.fixture(scope="module")
+def setup(sil):
+    import torch
+    b = wl.make_batch(256, (64, 32), 2, "q8", seed=0)
+    ws = [sil.upload_weight(f, buf, n, 256) for f, buf, n in b.jobs]
+    x = torch.from_numpy(b.x).cuda()
+    yield b, ws, x
+    for w in ws:
+        w.free()
+
+
+def _canaries(b, value=123.5):
+    import torch
+    return [torch.full((b.t, n), value, device="cuda") for _, _, n in b.jobs]
+
+
+def _expect(sil, code, fn):
+    before = sil.get_stats()
+    with pytest.raises(sil.ILError) as ei:
+        fn()
+    assert ei.value.code == code, str(ei.value)
+    after = sil.get_stats()
+    assert after["launches"] == before["launches"]
+    assert after["errors"] == before["errors"] + 1
+    return ei.value
+
+
+def _untouched(ys, value=123.5):
+    import torch
+    torch.cuda.synchronize()
+    return all(bool(torch.all(y == value)) for y in ys)
+
+
+def test_upload_rejects(sil):
+    q8 = wl.make_batch(64, (4,), 1, "q8").jobs[0][1]
+    ILError = sil.ILError
+    for fmt, buf, n_out, n_in, code in [
+        (7, q8, 4, 64, -3),                       # unknown format
+        ("q8", q8, 4, 48, -2),                    # Q needs n_in % 32 == 0
+        ("bf16", np.zeros(2 * 4 * 12, np.uint8), 4, 12, -2),   # bf16 needs n_in % 8 == 0
+        ("q8", q8, 0, 64, -2),                    # n_out >= 1
+        ("q8", q8, 4, 0, -2),
+        ("bf16", np.zeros(16, np.uint8), 1, 65536, -2),       # n_in limit
+    ]:
+        with pytest.raises(ILError) as ei:
+            sil.upload_weight(fmt, buf, n_out, n_in)
+        assert ei.value.code == code, (fmt, n_out, n_in, str(ei.value))
+    lib_ = sil.load()
+    assert lib_.il_upload_weight(0, None, 4, 64) is None
+    assert lib_.il_last_status() == -1
+
+
+def test_bad_batches_compute_nothing(sil, setup):
+    import torch
+    b, ws, x = setup
+    ys = _canaries(b)
+    jobs = list(zip(ws, ys))
+
+    # n_in mismatch: a weight of another width
+    other = sil.upload_weight("q8", wl.make_batch(128, (64,), 1, "q8").jobs[0][1], 64, 128)
+    _expect(sil, -2, lambda: sil.matmul_batch(x, [(other, ys[0]), (ws[1], ys[1])]))
+    other.free()
+    # n_out mismatch
+    _expect(sil, -2, lambda: sil.matmul_batch_ptr(x.data_ptr(), b.t, 256,
+                                                  [(ws[0], 63, ys[0].data_ptr())], 0))
+    # freed handle
+    dead = sil.upload_weight("q8", b.jobs[0][1], 64, 256)
+    h = dead.handle
+    dead.free()
+    _expect(sil, -4, lambda: sil.matmul_batch_ptr(x.data_ptr(), b.t, 256,
+                                                  [(h, 64, ys[0].data_ptr())], 0))
+    # forged handle
+    fake = ctypes.create_string_buffer(256)
+    _expect(sil, -4, lambda: sil.matmul_batch_ptr(x.data_ptr(), b.t, 256,
+                                                  [(ctypes.addressof(fake), 64, ys[0].data_ptr())], 0))
+    # null y / null x / misaligned x / misaligned y
+    _expect(sil, -1, lambda: sil.matmul_batch_ptr(x.data_ptr(), b.t, 256, [(ws[0], 64, 0)], 0))
+    _expect(sil, -1, lambda: sil.matmul_batch_ptr(0, b.t, 256, [(ws[0], 64, ys[0].data_ptr())], 0))
+    xb = torch.zeros(b.t * 256 + 4, device="cuda")
+    _expect(sil, -1, lambda: sil.matmul_batch_ptr(xb.data_ptr() + 4, b.t, 256,
+                                                  [(ws[0], 64, ys[0].data_ptr())], 0))
+    _expect(sil, -1, lambda: sil.matmul_batch_ptr(x.data_ptr(), b.t, 256,
+                                                  [(ws[0], 64, ys[0].data_ptr() + 2)], 0))
+    # overlapping outputs, and y overlapping x
+    _expect(sil, -1, lambda: sil.matmul_batch_ptr(x.data_ptr(), b.t, 256,
+                                                  [(ws[0], 64, ys[0].data_ptr()),
+                                                   (ws[1], 32, ys[0].data_ptr() + 64)], 0))
+    _expect(sil, -1, lambda: sil.matmul_batch_ptr(x.data_ptr(), b.t, 256,
+                                                  [(ws[0], 64, x.data_ptr())], 0))
+    # negative sizes
+    _expect(sil, -1, lambda: sil.matmul_batch_ptr(x.data_ptr(), -1, 256,
+                                                  [(ws[0], 64, ys[0].data_ptr())], 0))
+    # one bad job among good ones: nothing at all is computed
+    _expect(sil, -2, lambda: sil.matmul_batch_ptr(x.data_ptr(), b.t, 256,
+                                                  [(ws[0], 64, ys[0].data_ptr()),
+                                                   (ws[1], 31, ys[1].data_ptr())], 0))
+    assert _untouched(ys)
+
+
+def test_noops(sil, setup):
+    b, ws, x = setup
+    ys = _canaries(b)
+    before = sil.get_stats()
+    sil.matmul_batch_ptr(x.data_ptr(), 0, 256, [(ws[0], 64, ys[0].data_ptr())], 0)
+    sil.matmul_batch_ptr(x.data_ptr(), b.t, 256, [], 0)
+    assert sil.get_stats()["launches"] == before["launches"]
+    assert _untouched(ys)
+
+
+def test_weight_bytes_and_info(sil):
+    for fmt, n_out, n_in in (("bf16", 24, 64), ("q8", 24, 64), ("q4", 24, 64)):
+        buf = wl.make_batch(n_in, (n_out,), 1, fmt).jobs[0][1]
+        w = sil.upload_weight(fmt, buf, n_out, n_in)
+        assert w.bytes == buf.size == wl.weight_bytes(fmt, n_out, n_in)
+        f, o, i = ctypes.c_int(), ctypes.c_int64(), ctypes.c_int64()
+        assert sil.load().il_weight_info(w.handle, ctypes.byref(f), ctypes.byref(o),
+                                         ctypes.byref(i)) == 0
+        assert (f.value, o.value, i.value) == (sil.FORMATS[fmt], n_out, n_in)
+        w.free()
+    assert sil.load().il_weight_bytes(None) == -1
+
+
+def test_stats_count_work(sil, setup):
+    b, ws, x = setup
+    ys = _canaries(b)
+    sil.reset_stats()
+    sil.matmul_batch(x, list(zip(ws, ys)))
+    s = sil.get_stats()
+    assert s["batches"] == 1 and s["jobs"] == 2 and s["launches"] >= 1
+    assert s["weight_bytes"] == sum(w.bytes for w in ws)
+    assert s["flops"] == 2 * b.t * 256 * (64 + 32)
+
+
+def test_device_status_clean(sil):
+    sil.check_device_status()
+
+
+_ALLOC_SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r})
+import torch
+torch.cuda.set_device(0)
+import shared_input_linear_gb300 as sil
+import workloads as wl
+buf = wl.make_batch(64, (16,), 1, "q4").jobs[0][1]
+try:
+    sil.upload_weight("q4", buf, 16, 64)
+except sil.ILError as e:
+    print("CODE", e.code)
+    # a later upload also fails (the injected limit stays), and the process stays healthy
+    x = torch.ones(4, device="cuda")
+    torch.cuda.synchronize()
+    print("HEALTHY", float(x.sum()))
+"""
+
+
+def test_allocation_failure_injected(sil):
+    # IL_FAULT_ALLOC_FAIL_AFTER=1: the status word allocates, the weight's allocation fails
+    env = dict(os.environ, IL_FAULT_ALLOC_FAIL_AFTER="1")
+    out = subprocess.run([sys.executable, "-c", _ALLOC_SCRIPT.format(root=ROOT)], env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert "CODE -5" in out.stdout, out.stdout + out.stderr
+    assert "HEALTHY 4.0" in out.stdout, out.stdout + out.stderr

@@ -1,0 +1,269 @@
+"""GPU parity: the C-ABI path against the CPU oracle, element by element.
+
+Bar (per element): |y - y_ref| <= 8e-3 * sum_i |x_i w_i| + 1e-6; dequantised
+weights bit-exact; one-hot and integer-valued cases exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from gpu_util import GUARD, assert_parity, assert_parity_sampled, lib, run, upload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sil():
+    import torch
+    torch.cuda.set_device(0)
+    return lib()
+
+
+# ---------------------------------------------------------------------------
+# small and ragged shapes: the oracle computes every element
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("t", [1, 4])
+def test_tiny_workload(sil, t):
+    b = wl.make_workload_batch(wl.TINY, wl.TINY.batches[0], t, "bf16")
+    ys, guards = run(sil, b)
+    assert guards
+    assert_parity(b, ys, "tiny")
+
+
+SHAPES = [  # (n_in, n_outs) -- several tiles, ragged row tails, ragged K for the 128 padding
+    (32, (1, 7)),
+    (96, (129, 8, 3)),
+    (256, (1000,)),
+    (1056, (40, 17)),
+    (4128, (264, 9)),
+]
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+@pytest.mark.parametrize("t", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("n_in,n_outs", SHAPES)
+def test_small_shapes(sil, fmt, t, n_in, n_outs):
+    b = wl.make_batch(n_in, n_outs, t, fmt, seed=n_in + t)
+    ys, guards = run(sil, b)
+    assert guards, "a kernel wrote outside y"
+    assert_parity(b, ys, "small")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+@pytest.mark.parametrize("t", [9, 16, 17, 64, 129])
+def test_many_tokens(sil, fmt, t):
+    b = wl.make_batch(256, (136, 72, 5), t, fmt, seed=t)
+    ys, guards = run(sil, b)
+    assert guards
+    assert_parity(b, ys, "many tokens")
+
+
+def test_bf16_odd_k(sil):
+    # bf16 allows any n_in that is a multiple of 8
+    for n_in in (8, 40, 264):
+        b = wl.make_batch(n_in, (33, 16), 3, "bf16", seed=n_in)
+        ys, guards = run(sil, b)
+        assert guards
+        assert_parity(b, ys, "odd k")
+
+
+def test_mixed_formats_one_batch(sil):
+    import torch
+    n_in, t = 512, 4
+    b16 = wl.make_batch(n_in, (100,), t, "bf16", seed=1)
+    b8 = wl.make_batch(n_in, (64,), t, "q8", seed=1)
+    b4 = wl.make_batch(n_in, (48,), t, "q4", seed=1)
+    b = wl.BatchInputs("mixed", t, n_in, b16.x, b16.jobs + b8.jobs + b4.jobs)
+    ys, guards = run(sil, b)
+    assert guards
+    assert_parity(b, ys, "mixed")
+
+
+# ---------------------------------------------------------------------------
+# exact cases
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+def test_dequant_bit_exact(sil, fmt):
+    import torch
+    for n_out, n_in in ((13, 160), (256, 4096)):
+        b = wl.make_batch(n_in, (n_out,), 1, fmt, seed=7)
+        _, buf, _ = b.jobs[0]
+        w = sil.upload_weight(fmt, buf, n_out, n_in)
+        out = torch.full((n_out, n_in), float("nan"), device="cuda")
+        sil.dequantize_weight(w, out)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        ref = oracle.dequant(fmt, buf, n_out, n_in)
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), fmt
+        w.free()
+
+
+@pytest.mark.parametrize("fmt", ["q8", "q4"])
+def test_dequant_special_scales(sil, fmt):
+    import torch
+    # zero, subnormal, negative and huge scales must decode bit-exactly
+    n_out, n_in = 8, 192
+    rng = np.random.default_rng(5)
+    qmax = 127 if fmt == "q8" else 7
+    q = rng.integers(-qmax - 1, qmax + 1, size=(n_out, n_in))
+    d = np.array([0.0, 2.0 ** -130, -3.5, 1e30, 2.0 ** -149, 0.02 / 127] * 8,
+                 dtype=np.float32)[:n_out * (n_in // 32)].reshape(n_out, n_in // 32)
+    buf = wl.encode_q8(q, d) if fmt == "q8" else wl.encode_q4(q, d)
+    w = sil.upload_weight(fmt, buf, n_out, n_in)
+    out = torch.empty((n_out, n_in), device="cuda")
+    sil.dequantize_weight(w, out)
+    torch.cuda.synchronize()
+    ref = oracle.dequant(fmt, buf, n_out, n_in)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    w.free()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+@pytest.mark.parametrize("t_total", [8, 24])
+def test_one_hot_exact(sil, fmt, t_total):
+    # x rows are unit vectors: y[t] must equal column k_t of the dequantised weight exactly
+    n_out, n_in = 200, 1024 if fmt != "bf16" else 1000
+    b = wl.make_batch(n_in, (n_out, 24), 1, fmt, seed=3)
+    ks = np.linspace(0, n_in - 1, t_total).astype(int)
+    x = np.zeros((t_total, n_in), dtype=np.float32)
+    x[np.arange(t_total), ks] = 1.0
+    bb = wl.BatchInputs(fmt, t_total, n_in, x, b.jobs)
+    ys, _ = run(sil, bb)
+    for (f, buf, n), y in zip(b.jobs, ys):
+        deq = oracle.dequant(f, buf, n, n_in)
+        assert np.array_equal(y, deq[:, ks].T.astype(np.float32)), f
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+@pytest.mark.parametrize("t", [1, 8, 40])
+def test_integer_exact(sil, fmt, t):
+    # integer weights (scale 1) and small integer x: every partial sum is an exact integer
+    rng = np.random.default_rng(t)
+    n_in, n_outs = 512, (77, 8)
+    x = rng.integers(-4, 5, size=(t, n_in)).astype(np.float32)
+    jobs = []
+    for n in n_outs:
+        if fmt == "bf16":
+            import torch
+            wint = rng.integers(-8, 9, size=(n, n_in)).astype(np.float32)
+            jobs.append((fmt, wl.encode_bf16(wl.bf16_bits(torch.from_numpy(wint))), n))
+        else:
+            lo, hi = (-128, 128) if fmt == "q8" else (-8, 8)
+            q = rng.integers(lo, hi, size=(n, n_in))
+            d = np.ones((n, n_in // 32), dtype=np.float32)
+            jobs.append((fmt, wl.encode_q8(q, d) if fmt == "q8" else wl.encode_q4(q, d), n))
+    b = wl.BatchInputs(fmt, t, n_in, x, jobs)
+    ys, _ = run(sil, b)
+    for (f, buf, n), y in zip(jobs, ys):
+        y_ref, _ = oracle.linear(f, buf, n, n_in, x)
+        assert np.array_equal(y.astype(np.float64), y_ref), f
+
+
+def test_identity_bf16(sil):
+    import torch
+    n = 256
+    eye = wl.encode_bf16(wl.bf16_bits(torch.eye(n)))
+    for t in (1, 8):
+        x = wl.make_x(t, n, seed=2)
+        b = wl.BatchInputs("bf16", t, n, x, [("bf16", eye, n)])
+        ys, _ = run(sil, b)
+        # the decode path keeps x to ~16 bits: exact for W = I up to that split
+        assert np.all(np.abs(ys[0] - x) <= np.abs(x) * 2.0 ** -16)
+
+
+# ---------------------------------------------------------------------------
+# structural invariants
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", ["bf16", "q4"])
+@pytest.mark.parametrize("t", [1, 8, 33])
+def test_job_permutation(sil, fmt, t):
+    b = wl.make_batch(1024, (300, 64, 500), t, fmt, seed=11)
+    ws = upload(sil, b)
+    ys, _ = run(sil, b, weights=ws)
+    perm = [2, 0, 1]
+    bp = wl.BatchInputs(fmt, t, b.n_in, b.x, [b.jobs[i] for i in perm])
+    ysp, _ = run(sil, bp, weights=[ws[i] for i in perm])
+    for k, i in enumerate(perm):
+        assert np.array_equal(ysp[k], ys[i])
+    for w in ws:
+        w.free()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8"])
+@pytest.mark.parametrize("t", [4, 20])
+def test_batch_equals_single_jobs(sil, fmt, t):
+    b = wl.make_batch(2048, (1024, 256), t, fmt, seed=12)
+    ws = upload(sil, b)
+    ys, _ = run(sil, b, weights=ws)
+    for j, w in enumerate(ws):
+        bj = wl.BatchInputs(fmt, t, b.n_in, b.x, [b.jobs[j]])
+        yj, _ = run(sil, bj, weights=[w])
+        f, buf, n = b.jobs[j]
+        _, mag = oracle.linear(f, buf, n, b.n_in, b.x)
+        # same arithmetic up to the split of K over cluster ranks
+        assert np.all(np.abs(yj[0] - ys[j]) <= 1e-5 * mag + 1e-7)
+    for w in ws:
+        w.free()
+
+
+@pytest.mark.parametrize("t", [4, 12])
+def test_row_locality(sil, t):
+    import torch
+    b = wl.make_batch(1024, (256, 40), t, "q8", seed=13)
+    ws = upload(sil, b)
+    ys, _ = run(sil, b, weights=ws)
+    x2 = b.x.copy()
+    x2[1] *= -3.0
+    b2 = wl.BatchInputs("q8", t, b.n_in, x2, b.jobs)
+    ys2, _ = run(sil, b2, weights=ws)
+    for y, y2 in zip(ys, ys2):
+        keep = [i for i in range(t) if i != 1]
+        assert np.array_equal(y[keep], y2[keep])
+        assert not np.array_equal(y[1], y2[1])
+    for w in ws:
+        w.free()
+
+
+def test_linearity(sil):
+    b = wl.make_batch(768, (96,), 5, "q4", seed=14)
+    ws = upload(sil, b)
+    x1 = b.x
+    x2 = wl.make_x(5, 768, seed=15)
+    a = np.float32(0.75)
+    ya, _ = run(sil, wl.BatchInputs("q4", 5, 768, (a * x1 + x2).astype(np.float32), b.jobs), weights=ws)
+    y1, _ = run(sil, wl.BatchInputs("q4", 5, 768, x1, b.jobs), weights=ws)
+    y2, _ = run(sil, wl.BatchInputs("q4", 5, 768, x2, b.jobs), weights=ws)
+    _, mag1 = oracle.linear("q4", b.jobs[0][1], 96, 768, np.abs(x1))
+    _, mag2 = oracle.linear("q4", b.jobs[0][1], 96, 768, np.abs(x2))
+    tol = 2 * (8e-3 * (a * mag1 + mag2) + 1e-6)
+    assert np.all(np.abs(ya[0] - (a * y1[0] + y2[0])) <= tol)
+    for w in ws:
+        w.free()
+
+
+def test_stream_ordering(sil):
+    # work queued on a side stream completes in stream order and is correct
+    import torch
+    s = torch.cuda.Stream()
+    b = wl.make_batch(512, (64, 64), 3, "bf16", seed=16)
+    with torch.cuda.stream(s):
+        ys, guards = run(sil, b, stream=s)
+    assert guards
+    assert_parity(b, ys, "side stream")
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads (the benchmark's shapes and launch configuration)
+# ---------------------------------------------------------------------------
+FULL = [(w, bt, t, fmt) for w in (wl.DECODE_BF16, wl.DECODE_QUANT, wl.VOCAB, wl.PREFILL_BF16)
+        for bt in w.batches for t in w.ts for fmt in w.fmts]
+
+
+@pytest.mark.parametrize("w,bt,t,fmt", FULL,
+                         ids=[f"{w.name}-{bt.name}-t{t}-{fmt}" for w, bt, t, fmt in FULL])
+def test_full_size_sampled(sil, w, bt, t, fmt):
+    b = wl.make_workload_batch(w, bt, t, fmt)
+    ys, guards = run(sil, b)
+    assert guards
+    assert_parity_sampled(b, ys, what=f"{w.name}/{bt.name}")
