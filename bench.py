@@ -166,36 +166,15 @@ class Batch:
                 w.free()
 
 
-def _graph_event(torch):
-    # an event recorded inside a captured graph must be an "external" record node
-    return torch.cuda.Event(enable_timing=True, external=True)
-
-
-def graph_of(torch, sil, batches, steps: int, stream, copy0: int = 0):
-    """Capture `steps` steps (each: every batch once) with an external event after each batch."""
-    events = [_graph_event(torch) for _ in range(steps * len(batches) + 1)]
+def graph_of(torch, sil, batch, steps: int, stream, copy0: int = 0):
+    """Capture `steps` launches of one batch (rotating weight copies); kernels only."""
     g = torch.cuda.CUDAGraph()
     launches0 = sil.get_stats()["launches"]
     with torch.cuda.graph(g, stream=stream):
-        events[0].record(stream)
-        k = 1
         for s in range(steps):
-            for b in batches:
-                b.launch(sil, copy0 + s, stream)
-                events[k].record(stream)
-                k += 1
+            batch.launch(sil, copy0 + s, stream)
     launches = sil.get_stats()["launches"] - launches0
-    return g, events, launches
-
-
-def per_batch_us(events, n_batches, steps):
-    out = [[] for _ in range(n_batches)]
-    k = 0
-    for _ in range(steps):
-        for j in range(n_batches):
-            out[j].append(events[k].elapsed_time(events[k + 1]) * 1e3)
-            k += 1
-    return [statistics.mean(v) for v in out]
+    return g, launches
 
 
 def copies_for(batch_bytes: int) -> int:
@@ -217,32 +196,46 @@ def run_headline(sil, torch, args, dist, clocks: ClockSampler):
                 b.launch(sil, s, stream)
     torch.cuda.synchronize()
 
-    # graph of L steps (L divides K), replayed K/L times
+    # One graph per batch holding L launches (L divides K).  The timed region
+    # replays, K/L times, the q/k/v graph then the gate+up graph, with an event
+    # at each graph boundary: that gives the device time of every batch kind
+    # over the timed region without events between kernels.
     K = args.steps
     L = max(d for d in range(1, min(K, 200) + 1) if K % d == 0)
-    g, events, launches_per_graph = graph_of(torch, sil, batches, L, stream)
+    graphs = []
+    launches_per_rep = 0
+    for b in batches:
+        g, n = graph_of(torch, sil, b, L, stream)
+        graphs.append(g)
+        launches_per_rep += n
     reps = K // L
-    g.replay()  # upload + warm
+    with torch.cuda.stream(stream):
+        for g in graphs:  # upload + warm
+            g.replay()
     torch.cuda.synchronize()
 
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+             for _ in range(reps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    start.record(stream)
-    for _ in range(reps):
-        g.replay()
-    end.record(stream)
+    with torch.cuda.stream(stream):
+        for r in range(reps):
+            marks[r][0].record(stream)
+            for j, g in enumerate(graphs):
+                g.replay()
+                marks[r][j + 1].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     if dist is not None:
         dist.barrier()
     clocks.mark(t0, t1)
-    elapsed_ms = start.elapsed_time(end)
+    elapsed_ms = marks[0][0].elapsed_time(marks[-1][-1])
     ms_local = elapsed_ms / K
-    kern_us = per_batch_us(events, len(batches), L)
+    kern_us = [sum(marks[r][j].elapsed_time(marks[r][j + 1]) for r in range(reps)) * 1e3 / K
+               for j in range(len(graphs))]
+    launches_per_graph = launches_per_rep
 
     # e2e: host buffers, pinned, copies inside the timed region every step
     e2e = run_e2e(sil, torch, batches, args, stream)
@@ -304,17 +297,28 @@ def run_per_config(sil, torch, pk):
                     inp = wl.BatchInputs(fmt, t, bt.n_in, wl.make_x(t, bt.n_in, seed=0), base.jobs)
                     copies = copies_for(inp.weight_bytes)
                     b = Batch(sil, torch, inp, copies)
-                    with torch.cuda.stream(stream):
-                        for s in range(3):
-                            b.launch(sil, s, stream)
-                    torch.cuda.synchronize()
+                    try:
+                        with torch.cuda.stream(stream):
+                            for s in range(3):
+                                b.launch(sil, s, stream)
+                        torch.cuda.synchronize()
+                    except sil.ILError as err:
+                        out.append({"workload": w.name, "batch": bt.name, "fmt": fmt, "t": t,
+                                    "error": str(err)})
+                        b.free()
+                        continue
                     iters = max(copies, 8) if t <= 8 else max(2, min(copies, 4))
-                    g, events, _ = graph_of(torch, sil, [b], iters, stream)
-                    g.replay()
+                    g, _ = graph_of(torch, sil, b, iters, stream)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    with torch.cuda.stream(stream):
+                        g.replay()
+                        e0.record(stream)
+                        for _ in range(3):
+                            g.replay()
+                        e1.record(stream)
                     torch.cuda.synchronize()
-                    g.replay()
-                    torch.cuda.synchronize()
-                    us = per_batch_us(events, 1, iters)[0]
+                    us = e0.elapsed_time(e1) * 1e3 / (3 * iters)
                     gbs = inp.weight_bytes / (us * 1e-6) / 1e9
                     tfl = inp.flops / (us * 1e-6) / 1e12
                     e = {"workload": w.name, "batch": bt.name, "fmt": fmt, "t": t,
@@ -443,8 +447,9 @@ def main():
                 "config": dict(config, parallelism=f"replicas{world}" if world > 1 else "single",
                                l2=f"weights rotate over {head['copies']} resident copies "
                                   f"({head['copies'] * head['step_bytes'] / 1e9:.2f} GB > L2)",
-                               timing=f"CUDA graph of {head['graph_steps']} steps replayed, "
-                                      "CUDA events on the launching stream"),
+                               timing=f"CUDA graphs of {head['graph_steps']} launches replayed, "
+                                      "one graph per batch kind, CUDA events at graph boundaries "
+                                      "on the launching stream"),
                 "tflops": round(head["step_flops"] * world / (ms * 1e-3) / 1e12, 4),
                 "roofline": roof, "e2e": {k: (round(v, 3) if isinstance(v, float) else v)
                                           for k, v in e2e.items()},

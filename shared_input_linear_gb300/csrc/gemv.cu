@@ -21,6 +21,8 @@
 //    through distributed shared memory in a fixed rank order (deterministic).
 //  * CTAs are persistent: a cluster walks row blocks with a stride of the
 //    number of clusters, and the prefetch runs across row-block boundaries.
+//    Groups per warp and the K split are chosen so that the row blocks fill
+//    the resident clusters in whole rounds (a part-full last round idles SMs).
 #include <cooperative_groups.h>
 
 #include <mutex>
@@ -38,8 +40,10 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSliceK = 4096;  // columns of x staged per CTA (32 bytes each)
 
+// Not volatile: independent MMAs (different accumulators) may be interleaved by
+// the scheduler, which hides the tensor-pipe latency of each accumulate chain.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -330,17 +334,38 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
   DecodeParams p = pin;
   const int ck = chunk_k(fmt);
   const int spc = ck / 16;
-  // groups / rows
-  const int G = (p.total_groups + 15) / 16 >= num_sms ? 2 : 1;
+  // Choose groups per warp G and the K split C (cluster size) so that the
+  // (row block, K slice) tasks fill the resident CTA slots in whole rounds:
+  // persistent clusters take row blocks round-robin, so a last round that is
+  // only partly full leaves SMs idle.  A slice holds at most kMaxSliceK columns.
+  const int max_cps = kMaxSliceK / ck;
+  const int c_min = (p.n_chunks + max_cps - 1) / max_cps;
+  double best = -1.0;
+  int G = 1, C = c_min, cps = (p.n_chunks + c_min - 1) / c_min;
+  for (int g = 2; g >= 1; --g) {
+    const int rowblocks = (p.total_groups + kWarps * g - 1) / (kWarps * g);
+    for (int c = c_min; c <= 8 && c <= p.n_chunks; ++c) {
+      const int cp = (p.n_chunks + c - 1) / c;
+      const int ce = (p.n_chunks + cp - 1) / cp;
+      if (ce != c) continue;
+      const size_t sm = (size_t)cp * spc * 512 + (c > 1 ? 2 * kWarps * g * 64 * sizeof(float) : 0);
+      const int slots = (sm <= 100 * 1024 ? 2 : 1) * num_sms;
+      const int clusters = slots / c;
+      if (clusters < 1) continue;
+      const int rounds = (rowblocks + clusters - 1) / clusters;
+      const double eff = (double)rowblocks / ((double)rounds * clusters) * ((double)clusters * c / slots);
+      // prefer fewer K slices and more groups per warp unless clearly worse
+      const double score = eff * (1.0 - 0.03 * (c - 1)) * (g == 2 ? 1.02 : 1.0);
+      if (score > best) {
+        best = score;
+        G = g;
+        C = c;
+        cps = cp;
+      }
+    }
+  }
   const int gpb = kWarps * G;
   p.n_rowblocks = (p.total_groups + gpb - 1) / gpb;
-  // K split over a cluster: at least enough slices to keep a slice <= kMaxSliceK
-  // columns; more when there are too few row blocks to cover the SMs twice.
-  const int max_cps = kMaxSliceK / ck;
-  int C = (p.n_chunks + max_cps - 1) / max_cps;
-  while (C < 8 && C < p.n_chunks && p.n_rowblocks * C < 2 * num_sms) ++C;
-  int cps = (p.n_chunks + C - 1) / C;
-  C = (p.n_chunks + cps - 1) / cps;
   if (C > 8) return cudaErrorInvalidValue;
   p.slices = C;
   p.chunks_per_slice = cps;
@@ -374,7 +399,13 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
     if (it != g_occ.end()) {
       resident = it->second;
     } else {
-      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      // Allow the largest slice once per kernel: a smaller value set later would
+      // make a cached larger configuration fail to launch.
+      int optin = 0;
+      cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+      if (e != cudaSuccess) return e;
+      if ((int)smem > optin) return cudaErrorInvalidValue;
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
       if (e != cudaSuccess) return e;
       if (cluster) {
         cfg.gridDim = dim3(C * p.n_rowblocks);

@@ -51,6 +51,33 @@ def test_small_shapes(sil, fmt, t, n_in, n_outs):
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+@pytest.mark.parametrize("t", [1, 3, 8])
+@pytest.mark.parametrize("n_in,n_outs", [(512, (1217, 7)), (1024, (2400, 130, 64)),
+                                         (256, (9000,)), (4096, (1000, 24))])
+def test_uneven_row_blocks(sil, fmt, t, n_in, n_outs):
+    # more row groups than SMs and not a multiple of the row block: partial row
+    # blocks, K split over clusters, and job boundaries inside row blocks
+    b = wl.make_batch(n_in, n_outs, t, fmt, seed=n_in * 7 + t)
+    ys, guards = run(sil, b)
+    assert guards
+    assert_parity(b, ys, "cut groups")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q4"])
+def test_repeatable_bits(sil, fmt):
+    # partial sums over K slices are combined in a fixed order: repeated calls give identical bits
+    b = wl.make_batch(2048, (3000, 1000), 5, fmt, seed=99)
+    ws = upload(sil, b)
+    first, _ = run(sil, b, weights=ws)
+    for _ in range(3):
+        again, _ = run(sil, b, weights=ws)
+        for y0, y1 in zip(first, again):
+            assert np.array_equal(y0.view(np.uint32), y1.view(np.uint32))
+    for w in ws:
+        w.free()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
 @pytest.mark.parametrize("t", [9, 16, 17, 64, 129])
 def test_many_tokens(sil, fmt, t):
     b = wl.make_batch(256, (136, 72, 5), t, fmt, seed=t)
@@ -240,6 +267,16 @@ def test_linearity(sil):
     assert np.all(np.abs(ya[0] - (a * y1[0] + y2[0])) <= tol)
     for w in ws:
         w.free()
+
+
+def test_alternating_launch_configurations(sil):
+    # the same kernel variant launched with shrinking and growing shared-memory slices
+    for n_in, n_outs in ((4096, (4096, 1024)), (256, (512, 256)), (4096, (4096, 1024)),
+                         (12288, (512,)), (256, (64,)), (12288, (512,))):
+        b = wl.make_batch(n_in, n_outs, 1, "bf16", seed=n_in)
+        ys, guards = run(sil, b)
+        assert guards
+        assert_parity_sampled(b, ys, n_samples=64, what=f"n_in={n_in}")
 
 
 def test_stream_ordering(sil):
