@@ -1,0 +1,443 @@
+// gemm.cu -- tensor-core path for large token counts: x cast once to bf16,
+// then one persistent tcgen05 GEMM launch over every job of the batch.
+//
+// For each job j (oxinfer src/gpu.rs, struct `Job` / `Backend::matmul`):
+//     y_j[t][o] = sum_k x_bf16[t][k] * W_j[o][k]      (fp32 accumulate)
+//
+// Tile: BM = 128 weight rows (MMA M) x BN tokens (MMA N) x BK = 64 columns per
+// pipeline stage.  Both operands are K-major in HBM (W is [n_out][n_in], x is
+// [t][n_in]) and arrive by TMA with the 128-byte swizzle that the tcgen05
+// shared-memory descriptors read directly.  The accumulator lives in tensor
+// memory (TMEM): 128 lanes = weight rows, BN columns = tokens, double
+// buffered so the epilogue of one tile overlaps the MMAs of the next.  With
+// TMEM lane = output column o, a warp's 32 lanes write 32 consecutive floats
+// of y[t][.], so the epilogue stores are coalesced without a transpose.
+//
+// Warp roles (6 warps): 0 = TMA producer, 1 = TMEM allocator + MMA issuer,
+// 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+// Every mbarrier wait is bounded; a wait that gives up records an error code
+// in the device status word, raises a CTA-wide abort flag and lets every role
+// leave its loop; TMEM is always released before exit.
+#include <cuda.h>
+
+#include <cstring>
+
+#include "il_internal.cuh"
+
+namespace il {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;            // bf16 columns per stage: one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kThreadsGemm = 192;  // 6 warps
+constexpr unsigned long long kWaitLimitCycles = 2ull << 30;  // ~1 s at 2 GHz
+
+constexpr int kMaxGemmJobs = 8;
+
+struct __align__(64) GemmParams {
+  CUtensorMap wmap[kMaxGemmJobs];
+  CUtensorMap xmap;
+  float* y[kMaxGemmJobs];
+  int n_out[kMaxGemmJobs];
+  int tile_begin[kMaxGemmJobs + 1];  // prefix over jobs of m_tiles * n_tiles
+  int n_jobs;
+  int t;
+  int n_tiles_n;
+  int num_kb;
+  int total_tiles;
+  unsigned* status;
+};
+
+// ---- PTX wrappers -----------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred P1;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n"
+      "selp.b32 %0, 1, 0, P1;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: false (and the abort flag raised, the code recorded) on timeout
+// or when another role has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         unsigned* status, unsigned code) {
+  const long long start = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if ((unsigned long long)(clock64() - start) > kWaitLimitCycles) {
+      *abort_flag = 1;
+      atomicOr(status, code);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                           uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row swizzle atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);        // start address
+  d |= (uint64_t)1 << 16;                         // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset: next 8-row atom
+  d |= (uint64_t)1 << 46;                         // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                         // swizzle: 128 bytes
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void locate_tile(const GemmParams& p, int tile, int& job, int& mt, int& nt) {
+  int j = p.n_jobs - 1;
+  while (j > 0 && p.tile_begin[j] > tile) --j;
+  const int local = tile - p.tile_begin[j];
+  job = j;
+  mt = local / p.n_tiles_n;
+  nt = local - mt * p.n_tiles_n;
+}
+
+// Status codes of the bounded waits (or-ed into the device status word).
+constexpr unsigned kStProducer = 0x1;
+constexpr unsigned kStMma = 0x2;
+constexpr unsigned kStEpilogue = 0x4;
+
+template <int BN>
+__global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid_constant__ GemmParams p) {
+  constexpr uint32_t kABytes = kBM * kBK * 2;
+  constexpr uint32_t kBBytes = BN * kBK * 2;
+  constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;                // [kStages]
+  uint64_t* empty = bars + kStages;     // [kStages]
+  uint64_t* tfull = bars + 2 * kStages; // [2]
+  uint64_t* tempty = tfull + 2;         // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 4);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.xmap)) : "memory");
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < p.total_tiles && !*abort_flag; tile += gridDim.x) {
+        int job, mt, nt;
+        locate_tile(p, tile, job, mt, nt);
+        const CUtensorMap* wm = &p.wmap[job];
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.status, kStProducer)) break;
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_expect_tx(fb, kStageBytes);
+          const uint32_t a_dst = smem_u32(tiles + stage * kStageBytes);
+          tma_load_2d(a_dst, wm, kb * kBK, mt * kBM, fb);
+          tma_load_2d(a_dst + kABytes, &p.xmap, kb * kBK, nt * BN, fb);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < p.total_tiles && !*abort_flag; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t aphase = (it >> 1) & 1;
+        if (!mbar_wait(smem_u32(&tempty[acc]), aphase ^ 1, abort_flag, p.status, kStMma)) break;
+        tc_fence_after();
+        const uint32_t tmem_d = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, p.status, kStMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(tiles + stage * kStageBytes);
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            // advance 16 columns = 32 bytes inside the 128-byte swizzle row
+            tc_mma(tmem_d, smem_desc_sw128(a_addr + 32 * k), smem_desc_sw128(b_addr + 32 * k), idesc,
+                   (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&empty[stage]));  // frees the stage when these MMAs finish
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&tfull[acc]));  // accumulator ready for the epilogue
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t aphase = (it >> 1) & 1;
+      if (!mbar_wait(smem_u32(&tfull[acc]), aphase, abort_flag, p.status, kStEpilogue)) break;
+      tc_fence_after();
+      int job, mt, nt;
+      locate_tile(p, tile, job, mt, nt);
+      const int n_out = p.n_out[job];
+      float* y = p.y[job];
+      const int row = mt * kBM + quarter * 32 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c0, r);
+        const int tok0 = nt * BN + c0;
+        if (row < n_out) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int tok = tok0 + j;
+            if (tok < p.t) y[(int64_t)tok * n_out + row] = __uint_as_float(r[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// x fp32 [t][n_in] -> bf16 [t][n_in_pad] (round to nearest even), 0 in the padding.
+__global__ void cast_bf16_kernel(const float* __restrict__ x, int64_t t, int64_t n_in, int64_t n_in_pad,
+                                 __nv_bfloat16* __restrict__ out) {
+  const int64_t per_row = n_in_pad / 8;
+  const int64_t total = t * per_row;
+  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < total;
+       v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = v / per_row;
+    const int64_t k = (v - r * per_row) * 8;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (k < n_in) {  // n_in is a multiple of 8: the 8 columns are all inside or all outside
+      const float4 a = *reinterpret_cast<const float4*>(x + r * n_in + k);
+      const float4 b = *reinterpret_cast<const float4*>(x + r * n_in + k + 4);
+      __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y), h1 = __floats2bfloat162_rn(a.z, a.w);
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y), h3 = __floats2bfloat162_rn(b.z, b.w);
+      o.x = *reinterpret_cast<uint32_t*>(&h0);
+      o.y = *reinterpret_cast<uint32_t*>(&h1);
+      o.z = *reinterpret_cast<uint32_t*>(&h2);
+      o.w = *reinterpret_cast<uint32_t*>(&h3);
+    }
+    *reinterpret_cast<uint4*>(out + r * n_in_pad + k) = o;
+  }
+}
+
+// ---- host: tensor maps through the driver entry point (no libcuda link) -----
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// bf16 [rows][cols] row-major with row pitch `pitch` elements; box = box_cols x box_rows.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch, uint32_t box_cols,
+              uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {pitch * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int grid_cast(int64_t work) {
+  int64_t g = (work + 255) / 256;
+  if (g > 4096) g = 4096;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+cudaError_t launch_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_in_pad, __nv_bfloat16* out,
+                             cudaStream_t stream) {
+  cast_bf16_kernel<<<grid_cast(t * (n_in_pad / 8)), 256, 0, stream>>>(x, t, n_in, n_in_pad, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs,
+                             int n_jobs, cudaStream_t stream, int num_sms, unsigned* status, int* launches) {
+  constexpr int BN = 256;
+  constexpr size_t smem = (size_t)kStages * (kBM * kBK * 2 + BN * kBK * 2) + 1024 + 256;
+  static unsigned long long attr_set = 0;  // one bit per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !(attr_set & (1ull << dev))) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set |= 1ull << dev;
+  }
+  for (int j0 = 0; j0 < n_jobs; j0 += kMaxGemmJobs) {
+    const int nj = n_jobs - j0 < kMaxGemmJobs ? n_jobs - j0 : kMaxGemmJobs;
+    GemmParams p;
+    memset(&p, 0, sizeof p);
+    p.n_jobs = nj;
+    p.t = (int)t;
+    p.n_tiles_n = (int)((t + BN - 1) / BN);
+    p.num_kb = (int)(n_in_pad / kBK);
+    p.status = status;
+    if (!make_map(&p.xmap, xb, (uint64_t)n_in_pad, (uint64_t)t, (uint64_t)n_in_pad, kBK, BN))
+      return cudaErrorInvalidValue;
+    int tiles = 0;
+    for (int j = 0; j < nj; ++j) {
+      const PackedWeight& w = *jobs[j0 + j].w;
+      if (!make_map(&p.wmap[j], w.quants, (uint64_t)w.n_in_pad, (uint64_t)w.n_out_pad, (uint64_t)w.n_in_pad, kBK,
+                    kBM))
+        return cudaErrorInvalidValue;
+      p.y[j] = jobs[j0 + j].y;
+      p.n_out[j] = (int)w.n_out;
+      p.tile_begin[j] = tiles;
+      tiles += (int)((w.n_out + kBM - 1) / kBM) * p.n_tiles_n;
+    }
+    p.tile_begin[nj] = tiles;
+    p.total_tiles = tiles;
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    gemm_bf16_kernel<BN><<<grid, kThreadsGemm, smem, stream>>>(p);
+    if (launches) ++*launches;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace il

@@ -404,10 +404,33 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
     if (overlaps(sorted[i - 1].first, sorted[i - 1].second, sorted[i].first, sorted[i].second))
       return fail(IL_ERR_ARG, "il_matmul_batch: x and the y buffers must not overlap");
 
-  // ---- dispatch (per format; decode kernel for t <= 8 in token groups of 8)
+  // ---- dispatch: t > 8 bf16 jobs -> cast x once + tensor-core GEMM; everything
+  // else -> decode kernel (token groups of 8), one launch per format present.
   int launches = 0;
   cudaError_t e = cudaSuccess;
+  const bool use_gemm = t > 8;
+  if (use_gemm) {
+    std::vector<GemmJob> gj;
+    int64_t n_in_pad = 0;
+    for (int j = 0; j < n_jobs; ++j) {
+      const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[j].w);
+      if (w->format != IL_BF16) continue;
+      gj.push_back(GemmJob{w, jobs[j].y});
+      n_in_pad = w->n_in_pad;
+    }
+    if (!gj.empty()) {
+      void* xb = nullptr;
+      const int rc = get_scratch(dev, stream, (size_t)t * (size_t)n_in_pad * 2, &xb);
+      if (rc != IL_OK) return rc;
+      e = launch_cast_bf16(x, t, n_in, n_in_pad, static_cast<__nv_bfloat16*>(xb), stream);
+      if (e == cudaSuccess) ++launches;
+      if (e == cudaSuccess)
+        e = launch_gemm_bf16(static_cast<const __nv_bfloat16*>(xb), t, n_in_pad, gj.data(), (int)gj.size(), stream,
+                             ds->num_sms, ds->status, &launches);
+    }
+  }
   for (int fmt = IL_BF16; fmt <= IL_Q4 && e == cudaSuccess; ++fmt) {
+    if (use_gemm && fmt == IL_BF16) continue;
     std::vector<int> idx;
     for (int j = 0; j < n_jobs; ++j)
       if (reinterpret_cast<const PackedWeight*>(jobs[j].w)->format == fmt) idx.push_back(j);
