@@ -114,6 +114,30 @@ il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int
 int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
                     void* stream);
 
+/*
+ * il_matmul_batch_noalloc -- the pages have no counterpart of this entry point.
+ * Same arguments, checks, result and error behaviour as il_matmul_batch, but it
+ * never allocates device memory: for callers that cannot let a library call
+ * cudaMalloc, such as services that give all device memory to their own pool at
+ * start-up, or latency-critical threads for which cudaMalloc / cudaFree may
+ * block and synchronise the device.
+ *   - The bf16 copy of x used by the tensor-core path (t > 8, bf16 weights)
+ *     goes to a fixed 16 MiB device array inside the library, held by every
+ *     GPU that loads the library until the process exits.  A batch needing
+ *     more, t * round_up(n_in, 128) * 2 bytes > 16 MiB, is rejected with
+ *     IL_ERR_UNSUPPORTED (e.g. t = 2048 fits at n_in = 4096, not at 12288).
+ *   - The first call on a device looks up the array's device address and
+ *     clears the library's status word there (a synchronous step); make that
+ *     first call before any stream capture.
+ *   - Every call shares the one array: calls that overlap on the GPU (on
+ *     different streams, or from different threads) race and may corrupt each
+ *     other's results.  Serialise them, e.g. on one stream.
+ *   - A device-side wait of the tensor-core kernel that gives up records its
+ *     code in that status word and ends the kernel early.
+ */
+int il_matmul_batch_noalloc(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
+                            void* stream);
+
 /* Releases a handle and its device memory (synchronises the device).
  * NULL is ignored; an unknown pointer is ignored and counted as an error. */
 void il_free_weight(il_weight* w);

@@ -18,7 +18,7 @@ import threading
 import numpy as np
 
 __all__ = ["ILError", "Weight", "FORMATS", "IL_BF16", "IL_Q8", "IL_Q4", "load", "build",
-           "upload_weight", "matmul_batch", "matmul_batch_ptr", "free_weight", "weight_bytes",
+           "upload_weight", "matmul_batch", "matmul_batch_ptr", "matmul_batch_noalloc_ptr", "free_weight", "weight_bytes",
            "dequantize_weight", "check_device_status", "get_stats", "reset_stats", "last_error",
            "version", "LIB_PATH", "STATUS"]
 
@@ -75,6 +75,8 @@ def load() -> ctypes.CDLL:
         lib.il_upload_weight.restype = vp
         lib.il_matmul_batch.argtypes = [vp, i64, i64, ctypes.POINTER(_Job), ci, vp]
         lib.il_matmul_batch.restype = ci
+        lib.il_matmul_batch_noalloc.argtypes = [vp, i64, i64, ctypes.POINTER(_Job), ci, vp]
+        lib.il_matmul_batch_noalloc.restype = ci
         lib.il_free_weight.argtypes = [vp]
         lib.il_free_weight.restype = None
         lib.il_weight_bytes.argtypes = [vp]
@@ -178,6 +180,18 @@ def matmul_batch_ptr(x_ptr: int, t: int, n_in: int, jobs, stream_ptr: int) -> in
         arr[i].n_out = int(n_out)
         arr[i].y = int(y)
     return _check(load().il_matmul_batch(x_ptr, int(t), int(n_in), arr, len(jobs), stream_ptr))
+
+
+def matmul_batch_noalloc_ptr(x_ptr: int, t: int, n_in: int, jobs, stream_ptr: int) -> int:
+    """``il_matmul_batch_noalloc`` on raw device pointers (same ``jobs`` form as
+    :func:`matmul_batch_ptr`).  The library allocates no device memory for it;
+    see ``include/il.h`` for the fixed scratch limit."""
+    arr = (_Job * max(1, len(jobs)))()
+    for i, (w, n_out, y) in enumerate(jobs):
+        arr[i].w = w.handle if isinstance(w, Weight) else w
+        arr[i].n_out = int(n_out)
+        arr[i].y = int(y)
+    return _check(load().il_matmul_batch_noalloc(x_ptr, int(t), int(n_in), arr, len(jobs), stream_ptr))
 
 
 def matmul_batch(x, jobs, stream=None) -> None:

@@ -472,3 +472,68 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Helpers for entry points defined in other translation units (they read the
+// handle registry, the error state and the counters kept here).
+// ---------------------------------------------------------------------------
+namespace il {
+
+void api_clear_error() { clear_error(); }
+
+int api_fail(int code, const char* msg) { return fail(code, "%s", msg); }
+
+int api_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+
+// The same checks il_matmul_batch makes, on the calling thread's device `dev`;
+// on success fills `ws` with the weight of each job.
+int api_check_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs, int dev,
+                    std::vector<const PackedWeight*>* ws, uint64_t* wbytes, uint64_t* flops) {
+  if (t < 0 || t > kMaxT) return fail(IL_ERR_ARG, "t=%lld out of range", (long long)t);
+  if (n_jobs < 0 || n_jobs > kMaxJobs) return fail(IL_ERR_ARG, "n_jobs=%d out of range", n_jobs);
+  ws->clear();
+  *wbytes = 0;
+  *flops = 0;
+  if (t == 0 || n_jobs == 0) return IL_OK;
+  if (x == nullptr) return fail(IL_ERR_ARG, "x is NULL");
+  if (jobs == nullptr) return fail(IL_ERR_ARG, "jobs is NULL");
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return fail(IL_ERR_ARG, "x is not 16-byte aligned");
+  if (n_in < 1 || n_in > kMaxNIn) return fail(IL_ERR_SHAPE, "n_in=%lld out of range", (long long)n_in);
+  std::vector<std::pair<uintptr_t, uintptr_t>> ranges;
+  ranges.emplace_back(reinterpret_cast<uintptr_t>(x), reinterpret_cast<uintptr_t>(x) + (uintptr_t)(t * n_in * 4));
+  {
+    std::lock_guard<std::mutex> lk(g_reg_mu);
+    for (int j = 0; j < n_jobs; ++j) {
+      const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[j].w);
+      if (w == nullptr || g_registry.count(w) == 0 || w->magic != kWeightMagic)
+        return fail(IL_ERR_HANDLE, "job %d has an invalid weight handle", j);
+      if (w->device != dev) return fail(IL_ERR_HANDLE, "job %d weight lives on device %d", j, w->device);
+      if (w->n_in != n_in) return fail(IL_ERR_SHAPE, "job %d weight n_in=%lld, batch n_in=%lld", j,
+                                       (long long)w->n_in, (long long)n_in);
+      if (jobs[j].n_out != w->n_out) return fail(IL_ERR_SHAPE, "job %d n_out=%lld, weight n_out=%lld", j,
+                                                 (long long)jobs[j].n_out, (long long)w->n_out);
+      if (jobs[j].y == nullptr) return fail(IL_ERR_ARG, "job %d y is NULL", j);
+      if (reinterpret_cast<uintptr_t>(jobs[j].y) % 4 != 0) return fail(IL_ERR_ARG, "job %d y is not 4-byte aligned", j);
+      const uintptr_t y0 = reinterpret_cast<uintptr_t>(jobs[j].y);
+      ranges.emplace_back(y0, y0 + (uintptr_t)(t * w->n_out * 4));
+      ws->push_back(w);
+      *wbytes += (uint64_t)w->host_bytes;
+      *flops += 2ull * (uint64_t)t * (uint64_t)n_in * (uint64_t)w->n_out;
+    }
+  }
+  std::sort(ranges.begin(), ranges.end());
+  for (size_t i = 1; i < ranges.size(); ++i)
+    if (overlaps(ranges[i - 1].first, ranges[i - 1].second, ranges[i].first, ranges[i].second))
+      return fail(IL_ERR_ARG, "x and the y buffers must not overlap");
+  return IL_OK;
+}
+
+void api_count_batch(int n_jobs, int launches, uint64_t wbytes, uint64_t flops) {
+  g_stats.batches.fetch_add(1);
+  g_stats.jobs.fetch_add((uint64_t)n_jobs);
+  g_stats.launches.fetch_add((uint64_t)launches);
+  g_stats.weight_bytes.fetch_add(wbytes);
+  g_stats.flops.fetch_add(flops);
+}
+
+}  // namespace il
