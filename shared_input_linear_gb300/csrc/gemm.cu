@@ -20,6 +20,7 @@
 // leave its loop; TMEM is always released before exit.
 #include <cuda.h>
 
+#include <cstdlib>
 #include <cstring>
 
 #include "il_internal.cuh"
@@ -46,6 +47,7 @@ struct __align__(64) GemmParams {
   int n_tiles_n;
   int num_kb;
   int total_tiles;
+  int stall_producer;  // failure-detection test: the producer never loads, so the MMA wait runs out
   unsigned* status;
 };
 
@@ -216,10 +218,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // set-up above overlaps the previous kernel; x (bf16 copy) and y need it finished
+  grid_dep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && !p.stall_producer) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.xmap)) : "memory");
       int stage = 0;
       uint32_t phase = 0;
@@ -315,6 +319,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
 
   tc_fence_before();
   __syncthreads();
+  grid_dep_launch();
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
@@ -327,6 +332,7 @@ __global__ void cast_bf16_kernel(const float* __restrict__ x, int64_t t, int64_t
                                  __nv_bfloat16* __restrict__ out) {
   const int64_t per_row = n_in_pad / 8;
   const int64_t total = t * per_row;
+  grid_dep_wait();
   for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < total;
        v += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = v / per_row;
@@ -344,6 +350,7 @@ __global__ void cast_bf16_kernel(const float* __restrict__ x, int64_t t, int64_t
     }
     *reinterpret_cast<uint4*>(out + r * n_in_pad + k) = o;
   }
+  grid_dep_launch();
 }
 
 // ---- host: tensor maps through the driver entry point (no libcuda link) -----
@@ -390,8 +397,16 @@ int grid_cast(int64_t work) {
 
 cudaError_t launch_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_in_pad, __nv_bfloat16* out,
                              cudaStream_t stream) {
-  cast_bf16_kernel<<<grid_cast(t * (n_in_pad / 8)), 256, 0, stream>>>(x, t, n_in, n_in_pad, out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid_cast(t * (n_in_pad / 8)));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = kUsePdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, cast_bf16_kernel, x, t, n_in, n_in_pad, out);
 }
 
 cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs,
@@ -416,6 +431,11 @@ cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
     p.n_tiles_n = (int)((t + BN - 1) / BN);
     p.num_kb = (int)(n_in_pad / kBK);
     p.status = status;
+    // IL_TEST_STALL_TMA_PRODUCER=1 (failure-detection tests only): the TMA
+    // producer issues nothing, the MMA warp's bounded wait gives up after about
+    // a second, the kernel records IL_ERR_DEVICE_TIMEOUT's code and exits cleanly.
+    const char* stall = getenv("IL_TEST_STALL_TMA_PRODUCER");
+    p.stall_producer = (stall != nullptr && stall[0] == '1') ? 1 : 0;
     if (!make_map(&p.xmap, xb, (uint64_t)n_in_pad, (uint64_t)t, (uint64_t)n_in_pad, kBK, BN))
       return cudaErrorInvalidValue;
     int tiles = 0;
@@ -432,9 +452,18 @@ cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
     p.tile_begin[nj] = tiles;
     p.total_tiles = tiles;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    gemm_bf16_kernel<BN><<<grid, kThreadsGemm, smem, stream>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreadsGemm);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = kUsePdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN>, p);
     if (launches) ++*launches;
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

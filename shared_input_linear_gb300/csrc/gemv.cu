@@ -149,10 +149,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
     }
   };
 
-  // Start the weight stream before staging x so HBM is busy from the first cycle.
+  // Start the weight stream before staging x so HBM is busy from the first cycle;
+  // the weights do not depend on the previous kernel, x may.
 #pragma unroll
   for (int s = 0; s < P; ++s)
     if (s < total) load_next(qr[s], sr[s]);
+  grid_dep_wait();
 
   // ---- stage this CTA's K slice of x in fragment order (hi/lo split)
   for (int e = threadIdx.x; e < slots * 32; e += kThreads) {
@@ -290,6 +292,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
       }
     }
   }
+  // the next kernel may start on SMs this one leaves (it waits for our writes itself)
+  grid_dep_launch();
   if (CLUSTER) cg::this_cluster().sync();  // keep shared memory alive for remote readers
 }
 
@@ -376,7 +380,7 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
   if (fn == nullptr) return cudaErrorInvalidValue;
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -422,6 +426,15 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
   }
   const int nclusters = p.n_rowblocks < resident ? p.n_rowblocks : resident;
   cfg.gridDim = dim3(nclusters * C);
+  // Early launch behind the previous kernel pays off when this grid fills every
+  // resident slot; a smaller grid would be placed unevenly on the SMs that free
+  // up first, so it waits for the previous kernel as usual.
+  if (kUsePdl && nclusters == resident) {
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs += 1;
+  }
   cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p);
   if (launches) ++*launches;
   return e;

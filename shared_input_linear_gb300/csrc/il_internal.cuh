@@ -109,6 +109,19 @@ __device__ __forceinline__ uint32_t q4_pair_to_bf16x2(uint32_t word, int s) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
+// Programmatic dependent launch: kernels are launched so that the next kernel
+// on the stream may start while this one drains.  A kernel waits for the grid
+// before it (griddepcontrol.wait) before reading anything that grid may write
+// (x) or writing anything it may read (y); work on inputs fixed at upload time
+// (the weights) may run before the wait.  Without a preceding grid both are no-ops.
+#ifndef IL_NO_PDL
+constexpr bool kUsePdl = true;
+#else
+constexpr bool kUsePdl = false;
+#endif
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

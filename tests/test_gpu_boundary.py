@@ -187,3 +187,43 @@ def test_allocation_failure_injected(sil):
                          capture_output=True, text=True, timeout=300)
     assert "CODE -5" in out.stdout, out.stdout + out.stderr
     assert "HEALTHY 4.0" in out.stdout, out.stdout + out.stderr
+
+
+_TIMEOUT_SCRIPT = r"""
+import os, sys
+sys.path.insert(0, {root!r})
+import numpy as np
+import torch
+torch.cuda.set_device(0)
+import shared_input_linear_gb300 as sil
+import workloads as wl
+import oracle
+b = wl.make_batch(256, (128,), 16, "bf16", seed=3)
+w = sil.upload_weight("bf16", b.jobs[0][1], 128, 256)
+x = torch.from_numpy(b.x).cuda()
+y = torch.zeros(16, 128, device="cuda")
+os.environ["IL_TEST_STALL_TMA_PRODUCER"] = "1"
+sil.matmul_batch(x, [(w, y)])          # enqueues; the kernel's wait gives up after ~1 s
+try:
+    sil.check_device_status()
+    print("NO_TIMEOUT")
+except sil.ILError as e:
+    print("CODE", e.code)
+del os.environ["IL_TEST_STALL_TMA_PRODUCER"]
+sil.matmul_batch(x, [(w, y)])          # the context is still usable
+torch.cuda.synchronize()
+sil.check_device_status()
+y_ref, mag = oracle.linear("bf16", b.jobs[0][1], 128, 256, b.x)
+ok, worst, _ = oracle.check(y.cpu().numpy(), y_ref, mag)
+print("AFTER", ok)
+"""
+
+
+def test_bounded_wait_reports_timeout():
+    # A wait that nothing will satisfy (the TMA producer is told to issue nothing):
+    # the tensor-core kernel gives up after about a second, records the timeout in
+    # the device status word, and the next call on the same context is correct.
+    out = subprocess.run([sys.executable, "-c", _TIMEOUT_SCRIPT.format(root=ROOT)],
+                         capture_output=True, text=True, timeout=300)
+    assert "CODE -7" in out.stdout, out.stdout + out.stderr
+    assert "AFTER True" in out.stdout, out.stdout + out.stderr
