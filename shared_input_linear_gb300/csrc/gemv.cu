@@ -72,11 +72,14 @@ __device__ __forceinline__ int find_job(const DecodeParams& p, int gidx) {
   return j;
 }
 
-template <int FMT, int G, int P, bool CLUSTER>
+template <int FMT, int G, int B, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
   using F = Fmt<FMT>;
   constexpr int GPB = kWarps * G;
   constexpr int SVN = F::SV > 0 ? F::SV : 1;
+  constexpr int kWStep = FMT == IL_BF16 ? 64 : 512;  // bytes per chunk along a lane's stream
+  constexpr int kSStep = 16 * SVN;                   // floats per chunk along a q's scale stream
+  constexpr int NA = FMT == IL_BF16 ? 2 : 1;         // accumulator sets per group (independent MMA chains)
   extern __shared__ __align__(16) uint8_t smem[];
 
   const int lane = threadIdx.x & 31;
@@ -91,69 +94,65 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
     nclusters = gridDim.x / p.slices;
   }
   const int c_begin = rank * p.chunks_per_slice;
-  const int c_cnt = min(p.chunks_per_slice, p.n_chunks - c_begin);
+  const int c_cnt = min(p.chunks_per_slice, p.n_chunks - c_begin);  // a multiple of B
+  const int nb = c_cnt / B;                                          // batches per row block
   const int my_rbs = (p.n_rowblocks - cid + nclusters - 1) / nclusters;
-  const int total = my_rbs * c_cnt;
+  const int total = my_rbs * nb;                                     // batches of this warp
   const int slots = p.chunks_per_slice * F::SPC;
   uint4* xf = reinterpret_cast<uint4*>(smem);
   float* red = reinterpret_cast<float*>(smem + (size_t)slots * 512);
 
-  // ---- load cursor: base pointers of this warp's G groups in the row block being loaded
+  // ---- load cursor: base pointers of this warp's G groups in the row block
+  // being loaded.  A group past the last job (a partial row block) streams
+  // group 0 instead: its results are never stored, and the loads stay
+  // branch-free.
   const uint8_t* lw[G];
   const float* ls[G];
   auto set_load_rb = [&](int rbi) {
     const int rb = cid + rbi * nclusters;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const int gidx = rb * GPB + warp * G + g;
-      lw[g] = nullptr;
-      ls[g] = nullptr;
-      if (rbi < my_rbs && gidx < p.total_groups) {
-        const DecodeJob& jb = p.jobs[find_job(p, gidx)];
-        const int64_t lg = gidx - jb.group_begin;
-        if (FMT == IL_BF16) {
-          lw[g] = jb.w + ((lg * 8 + n) * jb.row_stride + (int64_t)c_begin * 32 + 8 * q) * 2;
-        } else {
-          lw[g] = jb.w + ((lg * jb.row_stride + c_begin) * 32 + lane) * 16;
-          ls[g] = jb.s + ((lg * jb.row_stride + c_begin) * 4 + q) * (4 * F::SV);
-        }
+      int gidx = rb * GPB + warp * G + g;
+      if (gidx >= p.total_groups) gidx = 0;
+      const DecodeJob& jb = p.jobs[find_job(p, gidx)];
+      const int64_t lg = gidx - jb.group_begin;
+      if (FMT == IL_BF16) {
+        lw[g] = jb.w + ((lg * 8 + n) * jb.row_stride + (int64_t)c_begin * 32 + 8 * q) * 2;
+      } else {
+        lw[g] = jb.w + ((lg * jb.row_stride + c_begin) * 32 + lane) * 16;
+        ls[g] = jb.s + ((lg * jb.row_stride + c_begin) * 4 + q) * (4 * F::SV);
       }
     }
   };
-  constexpr int kWStep = FMT == IL_BF16 ? 64 : 512;  // bytes per chunk along a lane's stream
-  constexpr int kSStep = 16 * SVN;                   // floats per chunk along a q's scale stream
-
-  uint4 qr[P][G];
-  uint4 sr[P][G][SVN];
-  int l_rbi = 0, l_cc = 0;
+  // Loads move in batches of B consecutive chunks per group, double buffered:
+  // a batch's loads leave back to back (DRAM page locality) and one batch is
+  // always in flight while the other is consumed.
+  int l_rb = 0, l_b = 0;
   set_load_rb(0);
-  auto load_next = [&](uint4 (&dq)[G], uint4 (&ds)[G][SVN]) {
+  auto load_batch = [&](uint4 (&dq)[B][G], uint4 (&ds)[B][G][SVN]) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (lw[g] != nullptr) {
-        dq[g] = __ldg(reinterpret_cast<const uint4*>(lw[g] + (int64_t)l_cc * kWStep));
+    for (int i = 0; i < B; ++i)
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        dq[i][g] = __ldg(reinterpret_cast<const uint4*>(lw[g] + (l_b * B + i) * kWStep));
         if (F::SV > 0) {
 #pragma unroll
           for (int v = 0; v < F::SV; ++v)
-            ds[g][v] = __ldg(reinterpret_cast<const uint4*>(ls[g] + (int64_t)l_cc * kSStep) + v);
+            ds[i][g][v] = __ldg(reinterpret_cast<const uint4*>(ls[g] + (l_b * B + i) * kSStep) + v);
         }
-      } else {
-        dq[g] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int v = 0; v < SVN; ++v) ds[g][v] = make_uint4(0, 0, 0, 0);
       }
-    }
-    if (++l_cc == c_cnt) {
-      l_cc = 0;
-      set_load_rb(++l_rbi);
+    if (++l_b == nb) {
+      l_b = 0;
+      set_load_rb(++l_rb);
     }
   };
 
+  uint4 qa[B][G], qb[B][G];
+  uint4 sa[B][G][SVN], sb[B][G][SVN];
   // Start the weight stream before staging x so HBM is busy from the first cycle;
   // the weights do not depend on the previous kernel, x may.
-#pragma unroll
-  for (int s = 0; s < P; ++s)
-    if (s < total) load_next(qr[s], sr[s]);
+  if (total > 0) load_batch(qa, sa);
+  if (total > 1) load_batch(qb, sb);
   grid_dep_wait();
 
   // ---- stage this CTA's K slice of x in fragment order (hi/lo split)
@@ -174,122 +173,137 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
   }
   __syncthreads();
 
-  float acc[G][4];
+  float acc[G][NA][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int a = 0; a < NA; ++a) acc[g][a][0] = acc[g][a][1] = acc[g][a][2] = acc[g][a][3] = 0.f;
 
-  int c_rbi = 0, c_cc = 0;
-  for (int f0 = 0; f0 < total; f0 += P) {
+  int c_rb = 0, c_b = 0;  // consume cursor
+  auto epilogue = [&]() {
+    const int rb = cid + c_rb * nclusters;
+    float v[G][2];
 #pragma unroll
-    for (int s = 0; s < P; ++s) {
-      if (f0 + s < total) {
-        uint4 cq[G];
-        uint4 cs[G][SVN];
+    for (int g = 0; g < G; ++g) {
+      float r[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          cq[g] = qr[s][g];
+      for (int a = 0; a < NA; ++a) {
 #pragma unroll
-          for (int v = 0; v < SVN; ++v) cs[g][v] = sr[s][g][v];
-        }
-        if (f0 + s + P < total) load_next(qr[s], sr[s]);
-
-        const uint4* xs = xf + (c_cc * F::SPC) * 32 + lane;
-        if (FMT == IL_BF16) {
-          const uint4 a0 = xs[0], a1 = xs[32];
+        for (int j = 0; j < 4; ++j) r[j] += acc[g][a][j];
+        acc[g][a][0] = acc[g][a][1] = acc[g][a][2] = acc[g][a][3] = 0.f;
+      }
+      v[g][0] = r[0] + r[2];  // token n, row 2q   (hi + lo parts of x)
+      v[g][1] = r[1] + r[3];  // token n, row 2q+1
+    }
+    if (!CLUSTER) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            mma_bf16(acc[g], a0, cq[g].x, cq[g].y);
-            mma_bf16(acc[g], a1, cq[g].z, cq[g].w);
-          }
-        } else if (FMT == IL_Q8) {
-#pragma unroll
-          for (int bb = 0; bb < 2; ++bb) {
-            const uint4 a0 = xs[(2 * bb) * 32], a1 = xs[(2 * bb + 1) * 32];
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const uint32_t w0 = bb == 0 ? cq[g].x : cq[g].z;
-              const uint32_t w1 = bb == 0 ? cq[g].y : cq[g].w;
-              float t4[4] = {0.f, 0.f, 0.f, 0.f};
-              uint32_t b0, b1;
-              q8_word_to_bf16x2(w0, b0, b1);
-              mma_bf16(t4, a0, b0, b1);
-              q8_word_to_bf16x2(w1, b0, b1);
-              mma_bf16(t4, a1, b0, b1);
-              const float d0 = __uint_as_float(bb == 0 ? cs[g][0].x : cs[g][0].y);  // row 2q
-              const float d1 = __uint_as_float(bb == 0 ? cs[g][0].z : cs[g][0].w);  // row 2q+1
-              acc[g][0] = fmaf(d0, t4[0], acc[g][0]);
-              acc[g][2] = fmaf(d0, t4[2], acc[g][2]);
-              acc[g][1] = fmaf(d1, t4[1], acc[g][1]);
-              acc[g][3] = fmaf(d1, t4[3], acc[g][3]);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const uint4 a0 = xs[(2 * w) * 32], a1 = xs[(2 * w + 1) * 32];
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const uint32_t word = w == 0 ? cq[g].x : (w == 1 ? cq[g].y : (w == 2 ? cq[g].z : cq[g].w));
-              float t4[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_bf16(t4, a0, q4_pair_to_bf16x2(word, 0), q4_pair_to_bf16x2(word, 4));
-              mma_bf16(t4, a1, q4_pair_to_bf16x2(word, 8), q4_pair_to_bf16x2(word, 12));
-              const uint4 s01 = cs[g][0], s23 = cs[g][SVN - 1];
-              const uint32_t d0b = w == 0 ? s01.x : (w == 1 ? s01.y : (w == 2 ? s01.z : s01.w));
-              const uint32_t d1b = w == 0 ? s23.x : (w == 1 ? s23.y : (w == 2 ? s23.z : s23.w));
-              const float d0 = __uint_as_float(d0b), d1 = __uint_as_float(d1b);
-              acc[g][0] = fmaf(d0, t4[0], acc[g][0]);
-              acc[g][2] = fmaf(d0, t4[2], acc[g][2]);
-              acc[g][1] = fmaf(d1, t4[1], acc[g][1]);
-              acc[g][3] = fmaf(d1, t4[3], acc[g][3]);
-            }
-          }
-        }
-
-        if (++c_cc == c_cnt) {  // ---- epilogue of one row block
-          c_cc = 0;
-          const int rb = cid + c_rbi * nclusters;
-          if (!CLUSTER) {
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const int gidx = rb * GPB + warp * G + g;
-              if (gidx < p.total_groups && n < p.t) {
-                const DecodeJob& jb = p.jobs[find_job(p, gidx)];
-                const int row0 = (gidx - jb.group_begin) * 8 + 2 * q;
-                float* y = jb.y + (int64_t)n * jb.n_out + row0;
-                if (row0 < jb.n_out) y[0] = acc[g][0] + acc[g][2];
-                if (row0 + 1 < jb.n_out) y[1] = acc[g][1] + acc[g][3];
-              }
-              acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
-            }
-          } else {
-            float* rbuf = red + (c_rbi & 1) * GPB * 64;
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const int gl = warp * G + g;
-              *reinterpret_cast<float2*>(rbuf + gl * 64 + n * 8 + 2 * q) =
-                  make_float2(acc[g][0] + acc[g][2], acc[g][1] + acc[g][3]);
-              acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
-            }
-            cg::cluster_group cluster = cg::this_cluster();
-            cluster.sync();
-            const int per = (GPB * 64 + p.slices - 1) / p.slices;
-            const int e_end = min(GPB * 64, (rank + 1) * per);
-            for (int e = rank * per + threadIdx.x; e < e_end; e += kThreads) {
-              const int gl = e >> 6, m = (e >> 3) & 7, r = e & 7;
-              const int gidx = rb * GPB + gl;
-              if (gidx < p.total_groups && m < p.t) {
-                float v = 0.f;
-                for (int src = 0; src < p.slices; ++src)
-                  v += cluster.map_shared_rank(rbuf, src)[e];
-                const DecodeJob& jb = p.jobs[find_job(p, gidx)];
-                const int row = (gidx - jb.group_begin) * 8 + r;
-                if (row < jb.n_out) jb.y[(int64_t)m * jb.n_out + row] = v;
-              }
-            }
-          }
-          ++c_rbi;
+      for (int g = 0; g < G; ++g) {
+        const int gidx = rb * GPB + warp * G + g;
+        if (gidx < p.total_groups && n < p.t) {
+          const DecodeJob& jb = p.jobs[find_job(p, gidx)];
+          const int row0 = (gidx - jb.group_begin) * 8 + 2 * q;
+          float* y = jb.y + (int64_t)n * jb.n_out + row0;
+          if (row0 < jb.n_out) y[0] = v[g][0];
+          if (row0 + 1 < jb.n_out) y[1] = v[g][1];
         }
       }
+    } else {
+      float* rbuf = red + (c_rb & 1) * GPB * 64;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        *reinterpret_cast<float2*>(rbuf + (warp * G + g) * 64 + n * 8 + 2 * q) = make_float2(v[g][0], v[g][1]);
+      cg::cluster_group cluster = cg::this_cluster();
+      cluster.sync();
+      const int per = (GPB * 64 + p.slices - 1) / p.slices;
+      const int e_end = min(GPB * 64, (rank + 1) * per);
+      for (int e = rank * per + threadIdx.x; e < e_end; e += kThreads) {
+        const int gl = e >> 6, m = (e >> 3) & 7, r = e & 7;
+        const int gidx = rb * GPB + gl;
+        if (gidx < p.total_groups && m < p.t) {
+          float s = 0.f;
+          for (int src = 0; src < p.slices; ++src) s += cluster.map_shared_rank(rbuf, src)[e];
+          const DecodeJob& jb = p.jobs[find_job(p, gidx)];
+          const int row = (gidx - jb.group_begin) * 8 + r;
+          if (row < jb.n_out) jb.y[(int64_t)m * jb.n_out + row] = s;
+        }
+      }
+    }
+  };
+
+  auto consume = [&](const uint4 (&cq)[B][G], const uint4 (&cs)[B][G][SVN]) {
+    const uint4* xb = xf + (c_b * B * F::SPC) * 32 + lane;
+#pragma unroll
+    for (int i = 0; i < B; ++i) {
+      const uint4* xs = xb + (i * F::SPC) * 32;
+      if (FMT == IL_BF16) {
+        const uint4 a0 = xs[0], a1 = xs[32];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          mma_bf16(acc[g][0], a0, cq[i][g].x, cq[i][g].y);
+          mma_bf16(acc[g][NA - 1], a1, cq[i][g].z, cq[i][g].w);
+        }
+      } else if (FMT == IL_Q8) {
+        // two independent 32-blocks: both first MMAs, then both second MMAs
+        const uint4 a0 = xs[0], a1 = xs[32], a2 = xs[64], a3 = xs[96];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float t4[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          uint32_t bq[4][2];
+          q8_word_to_bf16x2(cq[i][g].x, bq[0][0], bq[0][1]);
+          q8_word_to_bf16x2(cq[i][g].y, bq[1][0], bq[1][1]);
+          q8_word_to_bf16x2(cq[i][g].z, bq[2][0], bq[2][1]);
+          q8_word_to_bf16x2(cq[i][g].w, bq[3][0], bq[3][1]);
+          mma_bf16(t4[0], a0, bq[0][0], bq[0][1]);
+          mma_bf16(t4[1], a2, bq[2][0], bq[2][1]);
+          mma_bf16(t4[0], a1, bq[1][0], bq[1][1]);
+          mma_bf16(t4[1], a3, bq[3][0], bq[3][1]);
+          float* ac = acc[g][0];
+          const float d00 = __uint_as_float(cs[i][g][0].x), d01 = __uint_as_float(cs[i][g][0].y);  // row 2q
+          const float d10 = __uint_as_float(cs[i][g][0].z), d11 = __uint_as_float(cs[i][g][0].w);  // row 2q+1
+          ac[0] = fmaf(d00, t4[0][0], ac[0]);
+          ac[2] = fmaf(d00, t4[0][2], ac[2]);
+          ac[1] = fmaf(d10, t4[0][1], ac[1]);
+          ac[3] = fmaf(d10, t4[0][3], ac[3]);
+          ac[0] = fmaf(d01, t4[1][0], ac[0]);
+          ac[2] = fmaf(d01, t4[1][2], ac[2]);
+          ac[1] = fmaf(d11, t4[1][1], ac[1]);
+          ac[3] = fmaf(d11, t4[1][3], ac[3]);
+        }
+      } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {  // one 32-block per word
+          const uint4 a0 = xs[(2 * w) * 32], a1 = xs[(2 * w + 1) * 32];
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const uint32_t word = w == 0 ? cq[i][g].x : (w == 1 ? cq[i][g].y : (w == 2 ? cq[i][g].z : cq[i][g].w));
+            float t4[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_bf16(t4, a0, q4_pair_to_bf16x2(word, 0), q4_pair_to_bf16x2(word, 4));
+            mma_bf16(t4, a1, q4_pair_to_bf16x2(word, 8), q4_pair_to_bf16x2(word, 12));
+            const uint4 s0 = cs[i][g][0], s1 = cs[i][g][SVN - 1];
+            const float d0 = __uint_as_float(w == 0 ? s0.x : (w == 1 ? s0.y : (w == 2 ? s0.z : s0.w)));
+            const float d1 = __uint_as_float(w == 0 ? s1.x : (w == 1 ? s1.y : (w == 2 ? s1.z : s1.w)));
+            float* ac = acc[g][0];
+            ac[0] = fmaf(d0, t4[0], ac[0]);
+            ac[2] = fmaf(d0, t4[2], ac[2]);
+            ac[1] = fmaf(d1, t4[1], ac[1]);
+            ac[3] = fmaf(d1, t4[3], ac[3]);
+          }
+        }
+      }
+    }
+    if (++c_b == nb) {
+      c_b = 0;
+      epilogue();
+      ++c_rb;
+    }
+  };
+
+  for (int bi = 0; bi < total; bi += 2) {
+    consume(qa, sa);
+    if (bi + 2 < total) load_batch(qa, sa);
+    if (bi + 1 < total) {
+      consume(qb, sb);
+      if (bi + 3 < total) load_batch(qb, sb);
     }
   }
   // the next kernel may start on SMs this one leaves (it waits for our writes itself)
@@ -300,19 +314,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
 // ---------------------------------------------------------------------------
 // host side: plan + launch
 // ---------------------------------------------------------------------------
-// Prefetch depth: chunk loads in flight per warp, split over its G groups.
-template <int FMT>
-struct Tuning;
-template <> struct Tuning<IL_BF16> { static constexpr int kLoads = 8; };
-template <> struct Tuning<IL_Q8> { static constexpr int kLoads = 4; };
-template <> struct Tuning<IL_Q4> { static constexpr int kLoads = 4; };
+// Chunks per load batch (double buffered): the chunk count of every K slice is
+// a multiple of it.  Q4 carries 12 registers per chunk and group, so it takes
+// two chunks per batch with one group per warp and one with two.
+__host__ __device__ constexpr int batch_chunks(int fmt, int G) {
+  return fmt == IL_BF16 ? 4 : (fmt == IL_Q8 ? 2 : (G == 1 ? 2 : 1));
+}
 
 using KernelFn = void (*)(DecodeParams);
 
 template <int FMT, int G, bool CLUSTER>
 KernelFn kernel_for() {
-  constexpr int P = Tuning<FMT>::kLoads / G > 2 ? Tuning<FMT>::kLoads / G : 2;
-  return decode_kernel<FMT, G, P, CLUSTER>;
+  return decode_kernel<FMT, G, batch_chunks(FMT, G), CLUSTER>;
 }
 
 KernelFn select(int fmt, int G, bool cluster) {
@@ -345,11 +358,12 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
   const int max_cps = kMaxSliceK / ck;
   const int c_min = (p.n_chunks + max_cps - 1) / max_cps;
   double best = -1.0;
-  int G = 1, C = c_min, cps = (p.n_chunks + c_min - 1) / c_min;
+  int G = 1, C = -1, cps = 0;
   for (int g = 2; g >= 1; --g) {
     const int rowblocks = (p.total_groups + kWarps * g - 1) / (kWarps * g);
+    const int bc = batch_chunks(fmt, g);
     for (int c = c_min; c <= 8 && c <= p.n_chunks; ++c) {
-      const int cp = (p.n_chunks + c - 1) / c;
+      const int cp = ((p.n_chunks + c - 1) / c + bc - 1) / bc * bc;  // a multiple of the batch
       const int ce = (p.n_chunks + cp - 1) / cp;
       if (ce != c) continue;
       const size_t sm = (size_t)cp * spc * 512 + (c > 1 ? 2 * kWarps * g * 64 * sizeof(float) : 0);
@@ -368,9 +382,9 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
       }
     }
   }
+  if (C < 1 || C > 8 || p.n_chunks % batch_chunks(fmt, G) != 0) return cudaErrorInvalidValue;
   const int gpb = kWarps * G;
   p.n_rowblocks = (p.total_groups + gpb - 1) / gpb;
-  if (C > 8) return cudaErrorInvalidValue;
   p.slices = C;
   p.chunks_per_slice = cps;
   const bool cluster = C > 1;

@@ -16,7 +16,8 @@ namespace il {
 // Packed device layout
 // ---------------------------------------------------------------------------
 // Rows are padded to a multiple of 8 (one "row group", the n=8 side of the
-// decode MMA) and columns to a multiple of 128 (one Q4 chunk); padding is 0.
+// decode MMA) and columns to a multiple of 256 (two Q4 chunks, so every
+// format's chunk count is even); padding is 0.
 //
 // BF16: plain row-major u16 [n_out_pad][n_in_pad].  The decode kernel reads
 //   16 bytes (8 consecutive k) per lane; the tensor-core kernel tiles it with
@@ -28,7 +29,7 @@ namespace il {
 //   Scales are a separate chunk-major stream: for each (group, chunk) and each
 //   q = 0..3, the scales of rows 2q and 2q+1 for every 32-block of the chunk.
 constexpr int kGroupRows = 8;
-constexpr int kPadK = 128;
+constexpr int kPadK = 256;
 constexpr int kChunkBytes = 512;
 
 __host__ __device__ constexpr int chunk_k(int fmt) { return fmt == IL_BF16 ? 32 : (fmt == IL_Q8 ? 64 : 128); }
