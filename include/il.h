@@ -161,7 +161,9 @@ int il_dequantize_weight(const il_weight* w, float* dev_out, void* stream);
 
 /* Reads (and clears) the device-side status word that bounded waits in the
  * kernels set when they give up.  Synchronises `stream`.  Returns IL_OK, or
- * IL_ERR_DEVICE_TIMEOUT if a wait timed out since the last call. */
+ * IL_ERR_DEVICE_TIMEOUT if a wait timed out since the last call; in that case
+ * it also clears the library's split-K workspaces on the current device
+ * (synchronously), so that later batches start from a clean state. */
 int il_check_device_status(void* stream);
 
 /* Message of the last error on this thread ("" if none). */

@@ -47,6 +47,10 @@ struct __align__(64) GemmParams {
   int n_tiles_n;
   int num_kb;
   int total_tiles;
+  int splits;          // K slices per tile (split-K); units = total_tiles * splits
+  int kb_per_split;
+  float* ws;           // split-K partial tiles [tile][split][BN][BM] (splits > 1)
+  unsigned* counters;  // split-K arrivals per tile, zero before the launch
   int stall_producer;  // failure-detection test: the producer never loads, so the MMA wait runs out
   unsigned* status;
 };
@@ -89,7 +93,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                          unsigned* status, unsigned code) {
   const long long start = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (*abort_flag) return false;
+    // a phase that completed stays completed: re-check so that roles waiting on
+    // the same phase agree even when the abort flag rises meanwhile
+    if (*abort_flag) return mbar_try_wait(bar, parity);
     if ((unsigned long long)(clock64() - start) > kWaitLimitCycles) {
       *abort_flag = 1;
       atomicOr(status, code);
@@ -171,6 +177,16 @@ __device__ __forceinline__ void locate_tile(const GemmParams& p, int tile, int& 
   nt = local - mt * p.n_tiles_n;
 }
 
+// Work unit -> (tile, K block range).
+__device__ __forceinline__ void unit_range(const GemmParams& p, int unit, int& tile, int& split, int& kb0, int& kb1) {
+  tile = unit / p.splits;
+  split = unit - tile * p.splits;
+  kb0 = split * p.kb_per_split;
+  kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 // Status codes of the bounded waits (or-ed into the device status word).
 constexpr unsigned kStProducer = 0x1;
 constexpr unsigned kStMma = 0x2;
@@ -227,11 +243,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.xmap)) : "memory");
       int stage = 0;
       uint32_t phase = 0;
-      for (int tile = blockIdx.x; tile < p.total_tiles && !*abort_flag; tile += gridDim.x) {
-        int job, mt, nt;
+      const int units = p.total_tiles * p.splits;
+      for (int unit = blockIdx.x; unit < units && !*abort_flag; unit += gridDim.x) {
+        int tile, split, kb0, kb1, job, mt, nt;
+        unit_range(p, unit, tile, split, kb0, kb1);
         locate_tile(p, tile, job, mt, nt);
         const CUtensorMap* wm = &p.wmap[job];
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.status, kStProducer)) break;
           const uint32_t fb = smem_u32(&full[stage]);
           mbar_expect_tx(fb, kStageBytes);
@@ -252,14 +270,17 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int tile = blockIdx.x; tile < p.total_tiles && !*abort_flag; tile += gridDim.x, ++it) {
+      const int units = p.total_tiles * p.splits;
+      for (int unit = blockIdx.x; unit < units && !*abort_flag; unit += gridDim.x, ++it) {
+        int tile, split, kb0, kb1;
+        unit_range(p, unit, tile, split, kb0, kb1);
         const int acc = it & 1;
         const uint32_t aphase = (it >> 1) & 1;
         if (!mbar_wait(smem_u32(&tempty[acc]), aphase ^ 1, abort_flag, p.status, kStMma)) break;
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + acc * BN;
         bool ok = true;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, p.status, kStMma)) {
             ok = false;
             break;
@@ -271,7 +292,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
           for (int k = 0; k < kBK / 16; ++k) {
             // advance 16 columns = 32 bytes inside the 128-byte swizzle row
             tc_mma(tmem_d, smem_desc_sw128(a_addr + 32 * k), smem_desc_sw128(b_addr + 32 * k), idesc,
-                   (kb > 0 || k > 0) ? 1u : 0u);
+                   (kb > kb0 || k > 0) ? 1u : 0u);
           }
           tc_commit(smem_u32(&empty[stage]));  // frees the stage when these MMAs finish
           if (++stage == kStages) {
@@ -286,8 +307,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    volatile int* last_flag = abort_flag + 1;
+    const int units = p.total_tiles * p.splits;
     int it = 0;
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
+    for (int unit = blockIdx.x; unit < units; unit += gridDim.x, ++it) {
+      int tile, split, kb0, kb1;
+      unit_range(p, unit, tile, split, kb0, kb1);
       const int acc = it & 1;
       const uint32_t aphase = (it >> 1) & 1;
       if (!mbar_wait(smem_u32(&tfull[acc]), aphase, abort_flag, p.status, kStEpilogue)) break;
@@ -296,24 +321,67 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
       locate_tile(p, tile, job, mt, nt);
       const int n_out = p.n_out[job];
       float* y = p.y[job];
-      const int row = mt * kBM + quarter * 32 + lane;
+      const int lrow = quarter * 32 + lane;
+      const int row = mt * kBM + lrow;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      float* part = p.splits > 1 ? p.ws + ((size_t)tile * p.splits + split) * (BN * kBM) : nullptr;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(taddr + c0, r);
-        const int tok0 = nt * BN + c0;
-        if (row < n_out) {
+        if (part != nullptr) {
+          // partial tile stored [token][row]: each store of the warp is 128 contiguous bytes
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int tok = tok0 + j;
-            if (tok < p.t) y[(int64_t)tok * n_out + row] = __uint_as_float(r[j]);
+          for (int j = 0; j < 32; ++j) part[(c0 + j) * kBM + lrow] = __uint_as_float(r[j]);
+        } else {
+          const int tok0 = nt * BN + c0;
+          if (row < n_out) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int tok = tok0 + j;
+              if (tok < p.t) y[(int64_t)tok * n_out + row] = __uint_as_float(r[j]);
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));  // accumulator free for the MMA warp
+      if (part != nullptr) {
+        // split-K: the last K slice to arrive sums every slice's partial, in slice order
+        __threadfence();
+        epi_bar();
+        if (warp == 2 && lane == 0) {
+          const unsigned old = atomicAdd(p.counters + tile, 1u);
+          const int last = old == (unsigned)(p.splits - 1);
+          if (last) {
+            p.counters[tile] = 0u;
+            __threadfence();
+          }
+          *last_flag = last;
+        }
+        epi_bar();
+        if (*last_flag && row < n_out) {
+          const float* base = p.ws + (size_t)tile * p.splits * (BN * kBM) + lrow;
+          const int ntok = min(BN, p.t - nt * BN);
+#pragma unroll 1
+          for (int c0 = 0; c0 < ntok; c0 += 16) {
+            // 16 tokens at a time: independent loads in flight, slices summed in order
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+#pragma unroll 1
+            for (int s = 0; s < p.splits; ++s) {
+              const float* src = base + ((size_t)s * BN + c0) * kBM;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + j * kBM);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < ntok) y[(int64_t)(nt * BN + c0 + j) * n_out + row] = v[j];
+          }
+        }
+      }
     }
   }
 
@@ -409,9 +477,69 @@ cudaError_t launch_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_
   return cudaLaunchKernelEx(&cfg, cast_bf16_kernel, x, t, n_in, n_in_pad, out);
 }
 
+namespace {
+
+constexpr int kBN = 256;
+
+struct Plan {
+  int splits, kb_per_split, total_tiles;
+};
+
+// Split-K only when the tiles alone leave SMs idle: estimated time = tensor work
+// spread over whole waves of units + traffic of writing and summing partials.
+Plan plan_launch(int64_t t, int64_t n_in_pad, const GemmJob* jobs, int nj, int num_sms, bool allow_split) {
+  Plan pl{1, 0, 0};
+  const int n_tiles_n = (int)((t + kBN - 1) / kBN);
+  const int num_kb = (int)(n_in_pad / kBK);
+  int64_t sum_n_out = 0;
+  for (int j = 0; j < nj; ++j) {
+    pl.total_tiles += (int)((jobs[j].w->n_out + kBM - 1) / kBM) * n_tiles_n;
+    sum_n_out += jobs[j].w->n_out;
+  }
+  pl.kb_per_split = num_kb;
+  if (!allow_split) return pl;
+  const double flops = 2.0 * (double)t * (double)n_in_pad * (double)sum_n_out;
+  double best = 1e30;
+  // at most two slices: the partial-tile traffic of more slices costs more than it saves
+  for (int s = 1; s <= 2 && s <= num_kb / 4; ++s) {
+    const int kbps = (num_kb + s - 1) / s;
+    const int se = (num_kb + kbps - 1) / kbps;
+    const int64_t units = (int64_t)pl.total_tiles * se;
+    const int64_t waves = (units + num_sms - 1) / num_sms;
+    const double eff = (double)units / ((double)waves * num_sms);
+    const double est = flops / (1.5e15 * eff) + (se > 1 ? 2.0 * se * (double)t * sum_n_out * 4.0 / 5.0e12 : 0.0);
+    if (est < best * 0.97 || s == 1) {
+      if (s == 1 || est < best * 0.97) {
+        best = est;
+        pl.splits = se;
+        pl.kb_per_split = kbps;
+      }
+    }
+  }
+  return pl;
+}
+
+size_t counter_bytes(int tiles) { return ((size_t)tiles * sizeof(unsigned) + 255) / 256 * 256; }
+
+}  // namespace
+
+size_t gemm_workspace_bytes(int64_t t, int64_t n_in_pad, const GemmJob* jobs, int n_jobs, int num_sms) {
+  size_t need = 0;
+  for (int j0 = 0; j0 < n_jobs; j0 += kMaxGemmJobs) {
+    const int nj = n_jobs - j0 < kMaxGemmJobs ? n_jobs - j0 : kMaxGemmJobs;
+    const Plan pl = plan_launch(t, n_in_pad, jobs + j0, nj, num_sms, true);
+    if (pl.splits > 1) {
+      const size_t b = counter_bytes(pl.total_tiles) + (size_t)pl.total_tiles * pl.splits * kBN * kBM * sizeof(float);
+      if (b > need) need = b;
+    }
+  }
+  return need;
+}
+
 cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs,
-                             int n_jobs, cudaStream_t stream, int num_sms, unsigned* status, int* launches) {
-  constexpr int BN = 256;
+                             int n_jobs, cudaStream_t stream, int num_sms, unsigned* status, int* launches,
+                             void* ws, size_t ws_bytes) {
+  constexpr int BN = kBN;
   constexpr size_t smem = (size_t)kStages * (kBM * kBK * 2 + BN * kBK * 2) + 1024 + 256;
   static unsigned long long attr_set = 0;  // one bit per device
   int dev = 0;
@@ -424,13 +552,28 @@ cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
   }
   for (int j0 = 0; j0 < n_jobs; j0 += kMaxGemmJobs) {
     const int nj = n_jobs - j0 < kMaxGemmJobs ? n_jobs - j0 : kMaxGemmJobs;
+    Plan pl = plan_launch(t, n_in_pad, jobs + j0, nj, num_sms, ws != nullptr);
+    const size_t cbytes = counter_bytes(pl.total_tiles);
+    if (pl.splits > 1 &&
+        cbytes + (size_t)pl.total_tiles * pl.splits * BN * kBM * sizeof(float) > ws_bytes) {
+      pl.splits = 1;
+      pl.kb_per_split = (int)(n_in_pad / kBK);
+    }
     GemmParams p;
     memset(&p, 0, sizeof p);
     p.n_jobs = nj;
     p.t = (int)t;
     p.n_tiles_n = (int)((t + BN - 1) / BN);
     p.num_kb = (int)(n_in_pad / kBK);
+    p.splits = pl.splits;
+    p.kb_per_split = pl.kb_per_split;
     p.status = status;
+    if (pl.splits > 1) {
+      // counters are zero when the workspace is created and the last arriver of
+      // every tile puts its counter back to zero
+      p.counters = static_cast<unsigned*>(ws);
+      p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + cbytes);
+    }
     // IL_TEST_STALL_TMA_PRODUCER=1 (failure-detection tests only): the TMA
     // producer issues nothing, the MMA warp's bounded wait gives up after about
     // a second, the kernel records IL_ERR_DEVICE_TIMEOUT's code and exits cleanly.
@@ -451,7 +594,8 @@ cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
     }
     p.tile_begin[nj] = tiles;
     p.total_tiles = tiles;
-    const int grid = tiles < num_sms ? tiles : num_sms;
+    const int units = tiles * p.splits;
+    const int grid = units < num_sms ? units : num_sms;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

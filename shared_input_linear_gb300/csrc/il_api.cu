@@ -56,10 +56,13 @@ struct DeviceState {
 std::mutex g_dev_mu;
 std::map<int, DeviceState> g_devices;
 
-// Scratch for the bf16 copy of x (tensor-core path), one buffer per (device, stream).
+// Scratch of the tensor-core path, one set per (device, stream): the bf16 copy
+// of x, and the split-K workspace.
 struct Scratch {
   void* ptr = nullptr;
   size_t bytes = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
 };
 std::mutex g_scratch_mu;
 std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
@@ -157,6 +160,33 @@ int get_scratch(int dev, cudaStream_t stream, size_t bytes, void** out) {
     s.bytes = want;
   }
   *out = s.ptr;
+  return IL_OK;
+}
+
+int get_workspace(int dev, cudaStream_t stream, size_t bytes, void** out, size_t* got) {
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  Scratch& s = g_scratch[{dev, stream}];
+  if (s.ws_bytes < bytes) {
+    if (s.ws != nullptr) {
+      cudaError_t e = cudaStreamSynchronize(stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+      cudaFree(s.ws);
+      s.ws = nullptr;
+      s.ws_bytes = 0;
+    }
+    cudaError_t e = il_malloc(&s.ws, bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      s.ws = nullptr;
+      return fail(IL_ERR_OOM, "allocating %zu bytes of split-K workspace failed", bytes);
+    }
+    // the per-tile arrival counters at its start must be zero before first use
+    e = cudaMemsetAsync(s.ws, 0, bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
+    s.ws_bytes = bytes;
+  }
+  *out = s.ws;
+  *got = s.ws_bytes;
   return IL_OK;
 }
 
@@ -345,7 +375,16 @@ int il_check_device_status(void* stream) {
   if (e == cudaSuccess) e = cudaMemsetAsync(ds->status, 0, sizeof word, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "il_check_device_status");
-  if (word != 0) return fail(IL_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (code 0x%x)", word);
+  if (word != 0) {
+    // a kernel that gave up may have left split-K arrival counters behind: clear
+    // this device's workspaces so the next launches start from zero
+    {
+      std::lock_guard<std::mutex> lk(g_scratch_mu);
+      for (auto& kv : g_scratch)
+        if (kv.first.first == dev && kv.second.ws != nullptr) cudaMemset(kv.second.ws, 0, kv.second.ws_bytes);
+    }
+    return fail(IL_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (code 0x%x)", word);
+  }
   return IL_OK;
 }
 
@@ -422,11 +461,17 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
       void* xb = nullptr;
       const int rc = get_scratch(dev, stream, (size_t)t * (size_t)n_in_pad * 2, &xb);
       if (rc != IL_OK) return rc;
+      void* ws = nullptr;
+      size_t ws_bytes = gemm_workspace_bytes(t, n_in_pad, gj.data(), (int)gj.size(), ds->num_sms);
+      if (ws_bytes > 0) {
+        const int rc2 = get_workspace(dev, stream, ws_bytes, &ws, &ws_bytes);
+        if (rc2 != IL_OK) return rc2;
+      }
       e = launch_cast_bf16(x, t, n_in, n_in_pad, static_cast<__nv_bfloat16*>(xb), stream);
       if (e == cudaSuccess) ++launches;
       if (e == cudaSuccess)
         e = launch_gemm_bf16(static_cast<const __nv_bfloat16*>(xb), t, n_in_pad, gj.data(), (int)gj.size(), stream,
-                             ds->num_sms, ds->status, &launches);
+                             ds->num_sms, ds->status, &launches, ws, ws_bytes);
     }
   }
   for (int fmt = IL_BF16; fmt <= IL_Q4 && e == cudaSuccess; ++fmt) {

@@ -103,7 +103,9 @@ __device__ __forceinline__ void q8_word_to_bf16x2(uint32_t word, uint32_t& lo01,
 // bf16 0x4300 is 128 with a 7-bit integer mantissa; xor 8 maps the two's
 // complement nibble to q+8, and subtracting 136 leaves q exactly.
 __device__ __forceinline__ uint32_t q4_pair_to_bf16x2(uint32_t word, int s) {
-  const uint32_t v = ((word >> s) & 0x000F000Fu) ^ 0x43084308u;
+  // one three-input logic op: (a & 0x000F000F) ^ 0x43084308 (truth table 0x6A)
+  uint32_t v;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(v) : "r"(word >> s), "n"(0x000F000F), "n"(0x43084308));
   __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v);
   const __nv_bfloat162 bias = __floats2bfloat162_rn(136.0f, 136.0f);
   b = __hsub2(b, bias);
@@ -142,8 +144,12 @@ struct GemmJob {
 };
 // Tensor-core path for large t (bf16 weights): xb is x cast to bf16,
 // [t][n_in_pad], zero in the padding columns.
+// ws / ws_bytes: split-K workspace (counters, then fp32 partial tiles); with
+// nullptr the kernel never splits K.  gemm_workspace_bytes gives the size the
+// launch plan wants (0 when no launch splits K).
 cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad,
                              const GemmJob* jobs, int n_jobs, cudaStream_t stream, int num_sms,
-                             unsigned* status, int* launches);
+                             unsigned* status, int* launches, void* ws, size_t ws_bytes);
+size_t gemm_workspace_bytes(int64_t t, int64_t n_in_pad, const GemmJob* jobs, int n_jobs, int num_sms);
 
 }  // namespace il

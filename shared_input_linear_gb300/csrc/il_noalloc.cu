@@ -116,7 +116,7 @@ extern "C" int il_matmul_batch_noalloc(const float* x, int64_t t, int64_t n_in, 
     if (e == cudaSuccess) ++launches;
     if (e == cudaSuccess)
       e = launch_gemm_bf16(xb, t, n_in_pad, gj.data(), (int)gj.size(), stream, slot->num_sms, slot->status,
-                           &launches);
+                           &launches, nullptr, 0);
   }
   // decode path (t <= 8, or Q8/Q4 weights): needs no scratch
   for (int fmt = IL_BF16; fmt <= IL_Q4 && e == cudaSuccess; ++fmt) {
