@@ -57,13 +57,21 @@ std::mutex g_dev_mu;
 std::map<int, DeviceState> g_devices;
 
 // Scratch of the tensor-core path, one set per (device, stream): the bf16 copy
-// of x, and the split-K workspace.
+// of x, the split-K workspace, and bf16 copies of Q8/Q4 weights at prefill sizes.
 struct Scratch {
   void* ptr = nullptr;
   size_t bytes = 0;
   void* ws = nullptr;
   size_t ws_bytes = 0;
+  void* wq = nullptr;
+  size_t wq_bytes = 0;
 };
+
+// Token counts above which a batch takes the tensor-core path: bf16 weights as
+// they are; Q8/Q4 weights after a dequantisation to bf16 (worth its extra pass
+// over the weight only once the decode kernel would stream it three times).
+constexpr int64_t kGemmMinT = 9;
+constexpr int64_t kGemmMinTQuant = 17;
 std::mutex g_scratch_mu;
 std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
 
@@ -160,6 +168,29 @@ int get_scratch(int dev, cudaStream_t stream, size_t bytes, void** out) {
     s.bytes = want;
   }
   *out = s.ptr;
+  return IL_OK;
+}
+
+int get_wq(int dev, cudaStream_t stream, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  Scratch& s = g_scratch[{dev, stream}];
+  if (s.wq_bytes < bytes) {
+    if (s.wq != nullptr) {
+      cudaError_t e = cudaStreamSynchronize(stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+      cudaFree(s.wq);
+      s.wq = nullptr;
+      s.wq_bytes = 0;
+    }
+    cudaError_t e = il_malloc(&s.wq, bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      s.wq = nullptr;
+      return fail(IL_ERR_OOM, "allocating %zu bytes for bf16 copies of quantised weights failed", bytes);
+    }
+    s.wq_bytes = bytes;
+  }
+  *out = s.wq;
   return IL_OK;
 }
 
@@ -443,21 +474,49 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
     if (overlaps(sorted[i - 1].first, sorted[i - 1].second, sorted[i].first, sorted[i].second))
       return fail(IL_ERR_ARG, "il_matmul_batch: x and the y buffers must not overlap");
 
-  // ---- dispatch: t > 8 bf16 jobs -> cast x once + tensor-core GEMM; everything
-  // else -> decode kernel (token groups of 8), one launch per format present.
+  // ---- dispatch: large t -> cast x once + tensor-core GEMM (Q8/Q4 weights first
+  // dequantised to bf16 scratch); everything else -> decode kernel (token groups
+  // of 8), one launch per format present.
   int launches = 0;
   cudaError_t e = cudaSuccess;
-  const bool use_gemm = t > 8;
-  if (use_gemm) {
+  const bool gemm_bf16 = t >= kGemmMinT;
+  const bool gemm_quant = t >= kGemmMinTQuant;
+  std::vector<PackedWeight> deq;  // bf16 views of Q8/Q4 weights (host descriptors)
+  if (gemm_bf16) {
     std::vector<GemmJob> gj;
+    std::vector<int> qidx;
     int64_t n_in_pad = 0;
+    size_t wq_bytes = 0;
     for (int j = 0; j < n_jobs; ++j) {
       const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[j].w);
-      if (w->format != IL_BF16) continue;
-      gj.push_back(GemmJob{w, jobs[j].y});
       n_in_pad = w->n_in_pad;
+      if (w->format == IL_BF16) {
+        gj.push_back(GemmJob{w, jobs[j].y});
+      } else if (gemm_quant) {
+        qidx.push_back(j);
+        wq_bytes += (size_t)w->n_out_pad * (size_t)w->n_in_pad * 2;
+      }
     }
-    if (!gj.empty()) {
+    if (!qidx.empty()) {
+      void* wq = nullptr;
+      const int rcq = get_wq(dev, stream, wq_bytes, &wq);
+      if (rcq != IL_OK) return rcq;
+      deq.reserve(qidx.size());
+      size_t off = 0;
+      for (int j : qidx) {
+        const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[j].w);
+        PackedWeight v = *w;
+        v.format = IL_BF16;
+        v.quants = static_cast<uint8_t*>(wq) + off;
+        v.scales = nullptr;
+        off += (size_t)w->n_out_pad * (size_t)w->n_in_pad * 2;
+        if (e == cudaSuccess) e = launch_dequant_bf16(*w, reinterpret_cast<__nv_bfloat16*>(v.quants), stream);
+        if (e == cudaSuccess) ++launches;
+        deq.push_back(v);
+      }
+      for (size_t i = 0; i < qidx.size(); ++i) gj.push_back(GemmJob{&deq[i], jobs[qidx[i]].y});
+    }
+    if (e == cudaSuccess && !gj.empty()) {
       void* xb = nullptr;
       const int rc = get_scratch(dev, stream, (size_t)t * (size_t)n_in_pad * 2, &xb);
       if (rc != IL_OK) return rc;
@@ -475,7 +534,7 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
     }
   }
   for (int fmt = IL_BF16; fmt <= IL_Q4 && e == cudaSuccess; ++fmt) {
-    if (use_gemm && fmt == IL_BF16) continue;
+    if (fmt == IL_BF16 ? gemm_bf16 : gemm_quant) continue;
     std::vector<int> idx;
     for (int j = 0; j < n_jobs; ++j)
       if (reinterpret_cast<const PackedWeight*>(jobs[j].w)->format == fmt) idx.push_back(j);

@@ -133,6 +133,9 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 // ---------------------------------------------------------------------------
 cudaError_t launch_pack(const PackedWeight& w, const uint8_t* staging, cudaStream_t stream);
 cudaError_t launch_dequant(const PackedWeight& w, float* out, cudaStream_t stream);
+// Q8/Q4 weight -> bf16 [n_out_pad][n_in_pad] row-major (RNE of fp32(d*q)), for the
+// tensor-core path at prefill sizes.
+cudaError_t launch_dequant_bf16(const PackedWeight& w, __nv_bfloat16* out, cudaStream_t stream);
 cudaError_t launch_decode(int fmt, const DecodeParams& p, cudaStream_t stream, int num_sms,
                           int* launches);
 cudaError_t launch_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_in_pad,

@@ -104,6 +104,44 @@ __global__ void pack_q4_kernel(const uint8_t* __restrict__ src, uint8_t* __restr
   }
 }
 
+// Element (r, k) of a packed weight as fp32: bf16 widened exactly, Q8/Q4 as
+// fp32(d*q) -- the element decoders of the matmul kernels, then one multiply.
+__device__ __forceinline__ float packed_element(int fmt, const uint8_t* __restrict__ wq,
+                                                const float* __restrict__ ws, int64_t n_in_pad,
+                                                int64_t n_chunks, int64_t r, int64_t k) {
+  const int64_t g = r >> 3;
+  const int n = (int)(r & 7);
+  if (fmt == IL_BF16) {
+    const uint16_t b = reinterpret_cast<const uint16_t*>(wq)[r * n_in_pad + k];
+    return __uint_as_float((uint32_t)b << 16);
+  }
+  if (fmt == IL_Q8) {
+    const int64_t c = k / 64;
+    const int kk = (int)(k % 64);
+    const int i = kk / 16, q = (kk % 16) / 4, j = kk % 4;
+    const int lane = 4 * n + q;
+    const uint32_t word = reinterpret_cast<const uint32_t*>(wq)[((g * n_chunks + c) * 32 + lane) * 4 + i];
+    uint32_t p01, p23;
+    q8_word_to_bf16x2(word, p01, p23);
+    const uint32_t pr = (j < 2) ? p01 : p23;
+    const float qv = (j & 1) ? bf16_hi(pr) : bf16_lo(pr);
+    const int qs = n >> 1, blk = kk / 32;
+    const float d = ws[((g * n_chunks + c) * 4 + qs) * 4 + (n & 1) * 2 + blk];
+    return __fmul_rn(d, qv);
+  }
+  const int64_t c = k / 128;
+  const int kk = (int)(k % 128);
+  const int w = kk / 32, sub = (kk % 32) / 16, q = (kk % 16) / 4, j = kk % 4;
+  const int lane = 4 * n + q;
+  const uint32_t word = reinterpret_cast<const uint32_t*>(wq)[((g * n_chunks + c) * 32 + lane) * 4 + w];
+  const int p = sub * 2 + (j >> 1) + (j & 1) * 4;
+  const uint32_t pr = q4_pair_to_bf16x2(word, 4 * (p & 3));
+  const float qv = (p >> 2) ? bf16_hi(pr) : bf16_lo(pr);
+  const int qs = n >> 1;
+  const float d = ws[((g * n_chunks + c) * 4 + qs) * 8 + (n & 1) * 4 + w];
+  return __fmul_rn(d, qv);
+}
+
 // One thread per element of [n_out][n_in]; reads the packed layout back.
 __global__ void dequant_kernel(int fmt, const uint8_t* __restrict__ wq, const float* __restrict__ ws,
                                int64_t n_out, int64_t n_in, int64_t n_in_pad, int64_t n_chunks,
@@ -112,42 +150,70 @@ __global__ void dequant_kernel(int fmt, const uint8_t* __restrict__ wq, const fl
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = e / n_in, k = e % n_in;
+    out[e] = packed_element(fmt, wq, ws, n_in_pad, n_chunks, r, k);
+  }
+}
+
+// Q8/Q4 weight -> bf16 row-major [n_out_pad][n_in_pad] (round to nearest even of
+// fp32(d*q)), the layout the tensor-core kernel tiles.  One thread writes 8
+// consecutive columns of one row: they sit in two neighbouring lanes' words of
+// one chunk (4 columns each) and share one 32-block scale.
+__global__ void dequant_bf16_kernel(int fmt, const uint8_t* __restrict__ wq, const float* __restrict__ ws,
+                                    int64_t n_out_pad, int64_t n_in_pad, int64_t n_chunks,
+                                    __nv_bfloat16* __restrict__ out) {
+  const int64_t per_row = n_in_pad / 8;
+  const int64_t total = n_out_pad * per_row;
+  grid_dep_wait();  // the scratch may still be read by the previous kernel
+  const uint32_t* words = reinterpret_cast<const uint32_t*>(wq);
+  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < total;
+       v += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = v / per_row;
+    const int64_t k = (v - r * per_row) * 8;
     const int64_t g = r >> 3;
     const int n = (int)(r & 7);
-    float v;
-    if (fmt == IL_BF16) {
-      const uint16_t b = reinterpret_cast<const uint16_t*>(wq)[r * n_in_pad + k];
-      v = __uint_as_float((uint32_t)b << 16);
-    } else if (fmt == IL_Q8) {
-      const int64_t c = k / 64;
-      const int kk = (int)(k % 64);
-      const int i = kk / 16, q = (kk % 16) / 4, j = kk % 4;
-      const int lane = 4 * n + q;
-      const uint32_t word =
-          reinterpret_cast<const uint32_t*>(wq)[((g * n_chunks + c) * 32 + lane) * 4 + i];
-      uint32_t p01, p23;
-      q8_word_to_bf16x2(word, p01, p23);
-      const uint32_t pr = (j < 2) ? p01 : p23;
-      const float qv = (j & 1) ? bf16_hi(pr) : bf16_lo(pr);
-      const int qs = n >> 1, blk = kk / 32;
-      const float d = ws[((g * n_chunks + c) * 4 + qs) * 4 + (n & 1) * 2 + blk];
-      v = __fmul_rn(d, qv);
+    float q[8];
+    float d;
+    if (fmt == IL_Q8) {
+      const int64_t c = k >> 6;
+      const int kk = (int)(k & 63);
+      const int i = kk >> 4, q0 = (kk & 15) >> 2;  // q0 is 0 or 2
+      const int64_t base = ((g * n_chunks + c) * 32 + 4 * n + q0) * 4 + i;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // lanes q0 and q0 + 1
+        uint32_t p01, p23;
+        q8_word_to_bf16x2(words[base + 4 * h], p01, p23);
+        q[4 * h] = bf16_lo(p01);
+        q[4 * h + 1] = bf16_hi(p01);
+        q[4 * h + 2] = bf16_lo(p23);
+        q[4 * h + 3] = bf16_hi(p23);
+      }
+      d = ws[((g * n_chunks + c) * 4 + (n >> 1)) * 4 + (n & 1) * 2 + (kk >> 5)];
     } else {
-      const int64_t c = k / 128;
-      const int kk = (int)(k % 128);
-      const int w = kk / 32, sub = (kk % 32) / 16, q = (kk % 16) / 4, j = kk % 4;
-      const int lane = 4 * n + q;
-      const uint32_t word =
-          reinterpret_cast<const uint32_t*>(wq)[((g * n_chunks + c) * 32 + lane) * 4 + w];
-      const int p = sub * 2 + (j >> 1) + (j & 1) * 4;
-      const uint32_t pr = q4_pair_to_bf16x2(word, 4 * (p & 3));
-      const float qv = (p >> 2) ? bf16_hi(pr) : bf16_lo(pr);
-      const int qs = n >> 1;
-      const float d = ws[((g * n_chunks + c) * 4 + qs) * 8 + (n & 1) * 4 + w];
-      v = __fmul_rn(d, qv);
+      const int64_t c = k >> 7;
+      const int kk = (int)(k & 127);
+      const int w = kk >> 5, sub = (kk & 31) >> 4, q0 = (kk & 15) >> 2;
+      const int64_t base = ((g * n_chunks + c) * 32 + 4 * n + q0) * 4 + w;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t word = words[base + 4 * h];
+        const uint32_t p01 = q4_pair_to_bf16x2(word, 4 * (2 * sub));      // columns j = 0, 1
+        const uint32_t p23 = q4_pair_to_bf16x2(word, 4 * (2 * sub + 1));  // columns j = 2, 3
+        q[4 * h] = bf16_lo(p01);
+        q[4 * h + 1] = bf16_hi(p01);
+        q[4 * h + 2] = bf16_lo(p23);
+        q[4 * h + 3] = bf16_hi(p23);
+      }
+      d = ws[((g * n_chunks + c) * 4 + (n >> 1)) * 8 + (n & 1) * 4 + w];
     }
-    out[e] = v;
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(d, q[2 * i]), __fmul_rn(d, q[2 * i + 1]));
+      o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(out + r * n_in_pad + k) = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  grid_dep_launch();
 }
 
 int grid_for(int64_t work) {
@@ -175,6 +241,20 @@ cudaError_t launch_pack(const PackedWeight& w, const uint8_t* staging, cudaStrea
                                                          w.n_in, w.n_groups, w.n_chunks);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_bf16(const PackedWeight& w, __nv_bfloat16* out, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid_for(w.n_out_pad * (w.n_in_pad / 8)));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = kUsePdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, dequant_bf16_kernel, w.format, (const uint8_t*)w.quants, (const float*)w.scales,
+                            w.n_out_pad, w.n_in_pad, w.n_chunks, out);
 }
 
 cudaError_t launch_dequant(const PackedWeight& w, float* out, cudaStream_t stream) {

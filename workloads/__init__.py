@@ -69,11 +69,15 @@ PREFILL_BF16 = Workload("prefill_bf16_gateup_down", ("bf16",), (512, 2048),
                         (Batch("gate_up", 4096, (12288, 12288)),
                          Batch("down", 12288, (4096,))),
                         "prompt prefill, tensor-core regime")
+PREFILL_QUANT = Workload("prefill_quant_gateup_down", ("q8", "q4"), (512,),
+                         (Batch("gate_up", 4096, (12288, 12288)),
+                          Batch("down", 12288, (4096,))),
+                         "prompt prefill with quantised weights")
 VOCAB = Workload("vocab_projection", ("bf16", "q4"), (1, 8),
                  (Batch("vocab", 2560, (262144,)),),
                  "one very tall job")
 
-WORKLOADS = (TINY, DECODE_BF16, DECODE_QUANT, PREFILL_BF16, VOCAB)
+WORKLOADS = (TINY, DECODE_BF16, DECODE_QUANT, PREFILL_BF16, VOCAB, PREFILL_QUANT)
 BY_NAME = {w.name: w for w in WORKLOADS}
 
 
