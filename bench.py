@@ -423,12 +423,7 @@ def main():
     head = run_headline(sil, torch, args, dist, clocks)
     clk = clocks.stop()
 
-    ms = head["ms_per_step"]
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = head["step_bytes"] * world / (ms * 1e-3) / 1e9
+    ms, value = aggregate(head["ms_per_step"], head["step_bytes"], world, dist, "cuda")
 
     per_config = None
     if rank == 0 and world == 1 and not args.no_per_config:
@@ -476,6 +471,18 @@ def main():
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def aggregate(ms_local: float, step_bytes: int, world: int, dist=None, device="cpu"):
+    """Whole-job figures of N independent replicas: the slowest rank's time per step,
+    and the weight bytes of all ranks over that time (GB/s)."""
+    ms = ms_local
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, step_bytes * world / (ms * 1e-3) / 1e9
 
 
 def read_profile_traffic():
