@@ -13,8 +13,10 @@
 //    operand (8 rows), and the "A" operand holds 8 tokens of x split into a
 //    bf16 high part (rows 0-7) and the bf16 rounding of the remainder (rows
 //    8-15), so x keeps ~16 significant bits and one MMA serves any t <= 8.
-//    Q8 / Q4 weights are turned into exact bf16 integers in registers; the
-//    fp32 scale of each 32-block multiplies the fp32 partial of that block.
+//    Q8 / Q4 weights are turned into exact fp16 integers in registers and meet
+//    an fp16 hi/lo split of x scaled by a power of two per CTA (so no value of
+//    x overflows fp16); the fp32 scale of each 32-block multiplies the fp32
+//    partial of that block, and the power of two is undone in the epilogue.
 //  * x is staged once per CTA in shared memory, already in MMA fragment
 //    order.  When x's K range is large or the batch has few rows, K is split
 //    over the CTAs of a thread-block cluster, whose partial sums are reduced
@@ -48,6 +50,22 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint4& a, uint32_t
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+// (hi pair, lo pair) of two fp32 values in fp16: hi = f16_rn(v), lo = f16_rn(v - hi).
+__device__ __forceinline__ void split_pair_f16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // (hi pair, lo pair) of two fp32 values: hi = bf16_rn(v), lo = bf16_rn(v - hi).
@@ -156,22 +174,55 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
   grid_dep_wait();
 
   // ---- stage this CTA's K slice of x in fragment order (hi/lo split)
-  for (int e = threadIdx.x; e < slots * 32; e += kThreads) {
-    const int s = e >> 5, L = e & 31, m = L >> 2, qq = L & 3;
-    int k;
+  auto x_col = [&](int e, int& m, int& k) -> bool {
+    const int s = e >> 5, L = e & 31, qq = L & 3;
+    m = L >> 2;
     if (FMT == IL_BF16)
       k = 32 * (c_begin + (s >> 1)) + 8 * qq + 4 * (s & 1);
     else
       k = F::CK * c_begin + 16 * s + 4 * qq;
+    return m < p.t && k < p.n_in && s < c_cnt * F::SPC;
+  };
+  // Q8/Q4 (fp16 path): scale x by 2^-x_exp so that the slice's largest |x| lies in
+  // [2^13, 2^14), well inside fp16's range; the epilogue multiplies by 2^x_exp.
+  int x_exp = 0;
+  if (FMT != IL_BF16) {
+    __shared__ unsigned s_max_bits;
+    if (threadIdx.x == 0) s_max_bits = 0u;
+    __syncthreads();
+    float mx = 0.f;
+    for (int e = threadIdx.x; e < slots * 32; e += kThreads) {
+      int m, k;
+      if (x_col(e, m, k)) {
+        const float4 xv = *reinterpret_cast<const float4*>(p.x + (int64_t)m * p.x_row_stride + k);
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(xv.x), fabsf(xv.y)), fmaxf(fabsf(xv.z), fabsf(xv.w))));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0 && mx > 0.f) atomicMax(&s_max_bits, __float_as_uint(mx));  // non-negative: bits order as values
+    __syncthreads();
+    const float smax = __uint_as_float(s_max_bits);
+    x_exp = smax > 0.f ? max(-110, min(110, ilogbf(smax) - 13)) : 0;
+  }
+  const float x_scale = ldexpf(1.0f, -x_exp);
+  for (int e = threadIdx.x; e < slots * 32; e += kThreads) {
+    int m, k;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (m < p.t && k < p.n_in && s < c_cnt * F::SPC) {
+    if (x_col(e, m, k)) {
       const float4 xv = *reinterpret_cast<const float4*>(p.x + (int64_t)m * p.x_row_stride + k);
-      split_pair(xv.x, xv.y, v.x, v.y);
-      split_pair(xv.z, xv.w, v.z, v.w);
+      if (FMT == IL_BF16) {
+        split_pair(xv.x, xv.y, v.x, v.y);
+        split_pair(xv.z, xv.w, v.z, v.w);
+      } else {
+        split_pair_f16(xv.x * x_scale, xv.y * x_scale, v.x, v.y);
+        split_pair_f16(xv.z * x_scale, xv.w * x_scale, v.z, v.w);
+      }
     }
     xf[e] = v;
   }
   __syncthreads();
+  const float y_scale = ldexpf(1.0f, x_exp);
 
   float acc[G][NA][4];
 #pragma unroll
@@ -192,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
         for (int j = 0; j < 4; ++j) r[j] += acc[g][a][j];
         acc[g][a][0] = acc[g][a][1] = acc[g][a][2] = acc[g][a][3] = 0.f;
       }
-      v[g][0] = r[0] + r[2];  // token n, row 2q   (hi + lo parts of x)
-      v[g][1] = r[1] + r[3];  // token n, row 2q+1
+      v[g][0] = (r[0] + r[2]) * y_scale;  // token n, row 2q   (hi + lo parts of x)
+      v[g][1] = (r[1] + r[3]) * y_scale;  // token n, row 2q+1
     }
     if (!CLUSTER) {
 #pragma unroll
@@ -249,14 +300,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
         for (int g = 0; g < G; ++g) {
           float t4[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
           uint32_t bq[4][2];
-          q8_word_to_bf16x2(cq[i][g].x, bq[0][0], bq[0][1]);
-          q8_word_to_bf16x2(cq[i][g].y, bq[1][0], bq[1][1]);
-          q8_word_to_bf16x2(cq[i][g].z, bq[2][0], bq[2][1]);
-          q8_word_to_bf16x2(cq[i][g].w, bq[3][0], bq[3][1]);
-          mma_bf16(t4[0], a0, bq[0][0], bq[0][1]);
-          mma_bf16(t4[1], a2, bq[2][0], bq[2][1]);
-          mma_bf16(t4[0], a1, bq[1][0], bq[1][1]);
-          mma_bf16(t4[1], a3, bq[3][0], bq[3][1]);
+          q8_word_to_f16x2(cq[i][g].x, bq[0][0], bq[0][1]);
+          q8_word_to_f16x2(cq[i][g].y, bq[1][0], bq[1][1]);
+          q8_word_to_f16x2(cq[i][g].z, bq[2][0], bq[2][1]);
+          q8_word_to_f16x2(cq[i][g].w, bq[3][0], bq[3][1]);
+          mma_f16(t4[0], a0, bq[0][0], bq[0][1]);
+          mma_f16(t4[1], a2, bq[2][0], bq[2][1]);
+          mma_f16(t4[0], a1, bq[1][0], bq[1][1]);
+          mma_f16(t4[1], a3, bq[3][0], bq[3][1]);
           float* ac = acc[g][0];
           const float d00 = __uint_as_float(cs[i][g][0].x), d01 = __uint_as_float(cs[i][g][0].y);  // row 2q
           const float d10 = __uint_as_float(cs[i][g][0].z), d11 = __uint_as_float(cs[i][g][0].w);  // row 2q+1
@@ -277,8 +328,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
           for (int g = 0; g < G; ++g) {
             const uint32_t word = w == 0 ? cq[i][g].x : (w == 1 ? cq[i][g].y : (w == 2 ? cq[i][g].z : cq[i][g].w));
             float t4[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_bf16(t4, a0, q4_pair_to_bf16x2(word, 0), q4_pair_to_bf16x2(word, 4));
-            mma_bf16(t4, a1, q4_pair_to_bf16x2(word, 8), q4_pair_to_bf16x2(word, 12));
+            uint32_t pr[4];
+            q4_word_to_f16x2(word, pr);
+            mma_f16(t4, a0, pr[0], pr[1]);
+            mma_f16(t4, a1, pr[2], pr[3]);
             const uint4 s0 = cs[i][g][0], s1 = cs[i][g][SVN - 1];
             const float d0 = __uint_as_float(w == 0 ? s0.x : (w == 1 ? s0.y : (w == 2 ? s0.z : s0.w)));
             const float d1 = __uint_as_float(w == 0 ? s1.x : (w == 1 ? s1.y : (w == 2 ? s1.z : s1.w)));
@@ -422,8 +475,12 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
       int optin = 0;
       cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
       if (e != cudaSuccess) return e;
-      if ((int)smem > optin) return cudaErrorInvalidValue;
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, fn);
+      if (e != cudaSuccess) return e;
+      const int dyn_max = optin - (int)fa.sharedSizeBytes;  // static shared memory counts too
+      if ((int)smem > dyn_max) return cudaErrorInvalidValue;
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
       if (e != cudaSuccess) return e;
       if (cluster) {
         cfg.gridDim = dim3(C * p.n_rowblocks);

@@ -6,6 +6,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "../../include/il.h"
@@ -82,36 +83,6 @@ struct DecodeParams {
 // ---------------------------------------------------------------------------
 // Element decoders (shared by the decode kernel and the dequantise hook)
 // ---------------------------------------------------------------------------
-// Q8: one 32-bit word holds 4 int8; returns bf16x2 pairs (e0,e1) and (e2,e3),
-// each value exactly q (|q| <= 128 fits bf16's 8 significant bits).  Uses the
-// float with exponent 2^23: its low mantissa byte is an unsigned integer.
-__device__ __forceinline__ void q8_word_to_bf16x2(uint32_t word, uint32_t& lo01, uint32_t& hi23) {
-  const uint32_t u = word ^ 0x80808080u;  // q + 128 as unsigned bytes
-  const float2 m01 = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
-                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)));
-  const float2 m23 = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
-                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)));
-  const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
-  const float2 q01 = __fadd2_rn(m01, bias);
-  const float2 q23 = __fadd2_rn(m23, bias);
-  // q is exact in bf16, so the low 16 bits of each fp32 are zero: keep the high halves.
-  lo01 = __byte_perm(__float_as_uint(q01.x), __float_as_uint(q01.y), 0x7632);
-  hi23 = __byte_perm(__float_as_uint(q23.x), __float_as_uint(q23.y), 0x7632);
-}
-
-// Q4: nibbles at bit s and bit s+16 of `word` -> bf16x2 (low half from bit s).
-// bf16 0x4300 is 128 with a 7-bit integer mantissa; xor 8 maps the two's
-// complement nibble to q+8, and subtracting 136 leaves q exactly.
-__device__ __forceinline__ uint32_t q4_pair_to_bf16x2(uint32_t word, int s) {
-  // one three-input logic op: (a & 0x000F000F) ^ 0x43084308 (truth table 0x6A)
-  uint32_t v;
-  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(v) : "r"(word >> s), "n"(0x000F000F), "n"(0x43084308));
-  __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v);
-  const __nv_bfloat162 bias = __floats2bfloat162_rn(136.0f, 136.0f);
-  b = __hsub2(b, bias);
-  return *reinterpret_cast<uint32_t*>(&b);
-}
-
 // Programmatic dependent launch: kernels are launched so that the next kernel
 // on the stream may start while this one drains.  A kernel waits for the grid
 // before it (griddepcontrol.wait) before reading anything that grid may write
@@ -124,6 +95,50 @@ constexpr bool kUsePdl = false;
 #endif
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// fp16 decoders (the Q8/Q4 matmul path multiplies fp16 weights by fp16 x):
+// every |q| <= 128 is exact in fp16, and the fp16 with biased exponent 25 is
+// 1024 + its 10-bit mantissa, so one byte permute builds 1024 + u from a byte u.
+// Q8: word of 4 int8 -> fp16x2 pairs (e0,e1), (e2,e3), each exactly q.
+__device__ __forceinline__ void q8_word_to_f16x2(uint32_t word, uint32_t& p01, uint32_t& p23) {
+  const uint32_t u = word ^ 0x80808080u;                   // q + 128 as unsigned bytes
+  uint32_t a = __byte_perm(u, 0x64646464u, 0x5140);        // [u0, 0x64, u1, 0x64]
+  uint32_t b = __byte_perm(u, 0x64646464u, 0x5342);        // [u2, 0x64, u3, 0x64]
+  const __half2 bias = __floats2half2_rn(1152.0f, 1152.0f);  // 1024 + 128
+  __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+  p01 = *reinterpret_cast<uint32_t*>(&ha);
+  p23 = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+// Q4: the four fp16x2 pairs of one packed word, pair i made of the nibbles at
+// positions i and i+4 (bits 4i and 16+4i), each exactly q.  Nibbles at the
+// bottom of a byte give 1024 + (n^8); those at the top give 1024 + 16*(n^8),
+// which a multiply by 1/16 brings back, so only one shift is needed.
+__device__ __forceinline__ void q4_word_to_f16x2(uint32_t word, uint32_t (&pr)[4]) {
+  const uint32_t hi = word >> 8;
+  uint32_t v0, v1, v2, v3;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(v0) : "r"(word), "n"(0x000F000F), "n"(0x64086408));
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(v1) : "r"(word), "n"(0x00F000F0), "n"(0x64806480));
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(v2) : "r"(hi), "n"(0x000F000F), "n"(0x64086408));
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(v3) : "r"(hi), "n"(0x00F000F0), "n"(0x64806480));
+  const __half2 b0 = __floats2half2_rn(1032.0f, 1032.0f);      // 1024 + 8
+  const __half2 m1 = __floats2half2_rn(0.0625f, 0.0625f);      // 1/16
+  const __half2 b1 = __floats2half2_rn(-72.0f, -72.0f);        // -(64 + 8)
+  __half2 h0 = __hsub2(*reinterpret_cast<const __half2*>(&v0), b0);
+  __half2 h1 = __hfma2(*reinterpret_cast<const __half2*>(&v1), m1, b1);
+  __half2 h2 = __hsub2(*reinterpret_cast<const __half2*>(&v2), b0);
+  __half2 h3 = __hfma2(*reinterpret_cast<const __half2*>(&v3), m1, b1);
+  pr[0] = *reinterpret_cast<uint32_t*>(&h0);
+  pr[1] = *reinterpret_cast<uint32_t*>(&h1);
+  pr[2] = *reinterpret_cast<uint32_t*>(&h2);
+  pr[3] = *reinterpret_cast<uint32_t*>(&h3);
+}
+
+__device__ __forceinline__ float f16_lo(uint32_t v) {
+  return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }

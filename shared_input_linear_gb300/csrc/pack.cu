@@ -122,9 +122,9 @@ __device__ __forceinline__ float packed_element(int fmt, const uint8_t* __restri
     const int lane = 4 * n + q;
     const uint32_t word = reinterpret_cast<const uint32_t*>(wq)[((g * n_chunks + c) * 32 + lane) * 4 + i];
     uint32_t p01, p23;
-    q8_word_to_bf16x2(word, p01, p23);
+    q8_word_to_f16x2(word, p01, p23);
     const uint32_t pr = (j < 2) ? p01 : p23;
-    const float qv = (j & 1) ? bf16_hi(pr) : bf16_lo(pr);
+    const float qv = (j & 1) ? f16_hi(pr) : f16_lo(pr);
     const int qs = n >> 1, blk = kk / 32;
     const float d = ws[((g * n_chunks + c) * 4 + qs) * 4 + (n & 1) * 2 + blk];
     return __fmul_rn(d, qv);
@@ -135,8 +135,10 @@ __device__ __forceinline__ float packed_element(int fmt, const uint8_t* __restri
   const int lane = 4 * n + q;
   const uint32_t word = reinterpret_cast<const uint32_t*>(wq)[((g * n_chunks + c) * 32 + lane) * 4 + w];
   const int p = sub * 2 + (j >> 1) + (j & 1) * 4;
-  const uint32_t pr = q4_pair_to_bf16x2(word, 4 * (p & 3));
-  const float qv = (p >> 2) ? bf16_hi(pr) : bf16_lo(pr);
+  uint32_t prs[4];
+  q4_word_to_f16x2(word, prs);
+  const uint32_t pr = prs[p & 3];
+  const float qv = (p >> 2) ? f16_hi(pr) : f16_lo(pr);
   const int qs = n >> 1;
   const float d = ws[((g * n_chunks + c) * 4 + qs) * 8 + (n & 1) * 4 + w];
   return __fmul_rn(d, qv);
@@ -181,11 +183,11 @@ __global__ void dequant_bf16_kernel(int fmt, const uint8_t* __restrict__ wq, con
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // lanes q0 and q0 + 1
         uint32_t p01, p23;
-        q8_word_to_bf16x2(words[base + 4 * h], p01, p23);
-        q[4 * h] = bf16_lo(p01);
-        q[4 * h + 1] = bf16_hi(p01);
-        q[4 * h + 2] = bf16_lo(p23);
-        q[4 * h + 3] = bf16_hi(p23);
+        q8_word_to_f16x2(words[base + 4 * h], p01, p23);
+        q[4 * h] = f16_lo(p01);
+        q[4 * h + 1] = f16_hi(p01);
+        q[4 * h + 2] = f16_lo(p23);
+        q[4 * h + 3] = f16_hi(p23);
       }
       d = ws[((g * n_chunks + c) * 4 + (n >> 1)) * 4 + (n & 1) * 2 + (kk >> 5)];
     } else {
@@ -195,13 +197,14 @@ __global__ void dequant_bf16_kernel(int fmt, const uint8_t* __restrict__ wq, con
       const int64_t base = ((g * n_chunks + c) * 32 + 4 * n + q0) * 4 + w;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t word = words[base + 4 * h];
-        const uint32_t p01 = q4_pair_to_bf16x2(word, 4 * (2 * sub));      // columns j = 0, 1
-        const uint32_t p23 = q4_pair_to_bf16x2(word, 4 * (2 * sub + 1));  // columns j = 2, 3
-        q[4 * h] = bf16_lo(p01);
-        q[4 * h + 1] = bf16_hi(p01);
-        q[4 * h + 2] = bf16_lo(p23);
-        q[4 * h + 3] = bf16_hi(p23);
+        uint32_t prs[4];
+        q4_word_to_f16x2(words[base + 4 * h], prs);
+        const uint32_t p01 = prs[2 * sub];      // columns j = 0, 1
+        const uint32_t p23 = prs[2 * sub + 1];  // columns j = 2, 3
+        q[4 * h] = f16_lo(p01);
+        q[4 * h + 1] = f16_hi(p01);
+        q[4 * h + 2] = f16_lo(p23);
+        q[4 * h + 3] = f16_hi(p23);
       }
       d = ws[((g * n_chunks + c) * 4 + (n >> 1)) * 8 + (n & 1) * 4 + w];
     }
