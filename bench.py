@@ -345,6 +345,54 @@ def run_per_config(sil, torch, pk, only=None):
     return out
 
 
+def run_dispatch(sil, torch):
+    """Fixed cost of one submission (the pages quote ~0.15 ms per dispatch on Metal):
+    host time of an eager il_matmul_batch call, the same call made synchronous, the
+    device time of a graph-replayed tiny batch, and a call with no jobs."""
+    inp = wl.make_workload_batch(wl.TINY, wl.TINY.batches[0], 1, "bf16")
+    b = Batch(sil, torch, inp, 1)
+    stream = torch.cuda.Stream()
+    jobs = [(w, n, y.data_ptr()) for w, (_, _, n), y in zip(b.copies[0], inp.jobs, b.ys)]
+    sp = stream.cuda_stream
+    xp = b.x.data_ptr()
+    for _ in range(50):
+        sil.matmul_batch_ptr(xp, 1, inp.n_in, jobs, sp)
+    torch.cuda.synchronize()
+    n = 2000
+    t0 = time.perf_counter()
+    for _ in range(n):
+        sil.matmul_batch_ptr(xp, 1, inp.n_in, jobs, sp)
+    host_us = (time.perf_counter() - t0) / n * 1e6
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        sil.matmul_batch_ptr(xp, 1, inp.n_in, jobs, sp)
+        stream.synchronize()
+    sync_us = (time.perf_counter() - t0) / n * 1e6
+    t0 = time.perf_counter()
+    for _ in range(n):
+        sil.matmul_batch_ptr(xp, 1, inp.n_in, [], sp)
+    empty_us = (time.perf_counter() - t0) / n * 1e6
+    g, _ = graph_of(torch, sil, b, 100, stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    dev_us = e0.elapsed_time(e1) * 1e3 / 100
+    del g
+    b.free()
+    return {"workload": "tiny_bf16 (n_in 256 -> 512 + 256, t = 1), 2 jobs",
+            "host_us_per_call_async": round(host_us, 2),
+            "host_us_per_call_synchronous": round(sync_us, 2),
+            "host_us_per_empty_call": round(empty_us, 2),
+            "device_us_per_batch_graph": round(dev_us, 2),
+            "pages_metal_dispatch_us": 150.0}
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle on the host (baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
@@ -426,8 +474,10 @@ def main():
     ms, value = aggregate(head["ms_per_step"], head["step_bytes"], world, dist, "cuda")
 
     per_config = None
+    dispatch = None
     if rank == 0 and world == 1 and not args.no_per_config:
         per_config = run_per_config(sil, torch, pk)
+        dispatch = run_dispatch(sil, torch)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -466,7 +516,7 @@ def main():
                 "roofline": roof, "e2e": {k: (round(v, 3) if isinstance(v, float) else v)
                                           for k, v in e2e.items()},
                 "gpu_launches": head["launches"], "clocks": clk, "cpu_baseline": cpu,
-                "per_config": per_config}
+                "per_config": per_config, "dispatch": dispatch}
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
