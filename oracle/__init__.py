@@ -12,6 +12,11 @@ Q8/Q4) and the dot products accumulate in f64 with ``i`` ascending.
 
 The acceptance rule for a GPU result ``y`` is per element
 ``|y - y_ref| <= 8e-3 * mag + 1e-6`` with ``mag = sum_i |x_i * w_i|``.
+
+A fused gate+up job (oxinfer 0.0.1 ``src/drafter.rs``, ``Drafter::step``: the
+gate+up batch followed by ``gelu_mul``) is the two linear results followed by
+``h = gelu(g) * u`` in f64, gelu in the tanh form; its bar (``gate_up_tolerance``)
+propagates the bar of g and u through that product.
 """
 from __future__ import annotations
 
@@ -69,6 +74,10 @@ class Oracle:
         lib.oracle_linear_sampled.argtypes = [ctypes.c_int, vp, i64, i64, vp, i64, i64,
                                               vp, vp, vp, vp]
         lib.oracle_linear_sampled.restype = ctypes.c_int
+        lib.oracle_gelu.argtypes = [ctypes.c_double]
+        lib.oracle_gelu.restype = ctypes.c_double
+        lib.oracle_gelu_mul.argtypes = [vp, vp, i64, vp]
+        lib.oracle_gelu_mul.restype = None
         self.lib = lib
 
     def weight_bytes(self, fmt, n_out: int, n_in: int) -> int:
@@ -128,6 +137,30 @@ class Oracle:
         return y, mag
 
 
+    def gelu(self, g: float) -> float:
+        """gelu in the tanh form, in double."""
+        return float(self.lib.oracle_gelu(float(g)))
+
+    def gelu_mul(self, g: np.ndarray, u: np.ndarray) -> np.ndarray:
+        """``gelu(g) * u`` elementwise, f64 (the drafter's ``gelu_mul(&mut g, &u)``)."""
+        g = np.ascontiguousarray(g, dtype=np.float64)
+        u = np.ascontiguousarray(u, dtype=np.float64)
+        if g.shape != u.shape:
+            raise ValueError("g and u must have one shape")
+        h = np.empty_like(g)
+        self.lib.oracle_gelu_mul(_ptr(g), _ptr(u), g.size, _ptr(h))
+        return h
+
+    def gate_up(self, fmt, gate: np.ndarray, up: np.ndarray, n_out: int, n_in: int, x: np.ndarray):
+        """A gate+up job: the two linear results over one x, then ``gelu_mul``.
+
+        Returns ``(h, g, u, mag_g, mag_u)``, all f64 ``[t][n_out]``.
+        """
+        g, mag_g = self.linear(fmt, gate, n_out, n_in, x)
+        u, mag_u = self.linear(fmt, up, n_out, n_in, x)
+        return self.gelu_mul(g, u), g, u, mag_g, mag_u
+
+
 def _fmt(fmt) -> int:
     return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
 
@@ -168,6 +201,50 @@ def matmul_batch(x: np.ndarray, jobs):
     """
     n_in = x.shape[1]
     return [linear(fmt, w, n_out, n_in, x) for fmt, w, n_out in jobs]
+
+
+def gelu_mul(g, u) -> np.ndarray:
+    return default().gelu_mul(g, u)
+
+
+def gate_up(fmt, gate, up, n_out: int, n_in: int, x):
+    return default().gate_up(fmt, gate, up, n_out, n_in, x)
+
+
+# sup |gelu'(g)| over all g for the tanh form (about 1.12899, at |g| ~ 1.4185)
+GELU_LIPSCHITZ = 1.13
+# relative error allowed for evaluating gelu(g) * u in fp32 on top of the input errors
+GELU_EVAL_REL = 1e-5
+
+
+def gate_up_tolerance(g, u, mag_g, mag_u) -> np.ndarray:
+    """Allowed absolute error of ``h = gelu(g) * u`` when g and u each meet the bar.
+
+    With |g^ - g| <= eg = tol(mag_g) and |u^ - u| <= eu = tol(mag_u):
+    |gelu(g^) u^ - gelu(g) u| <= L eg (|u| + eu) + |gelu(g)| eu, L = sup |gelu'|,
+    plus a relative allowance for the fp32 evaluation of the product.
+    """
+    g = np.asarray(g, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    eg = tolerance(mag_g)
+    eu = tolerance(mag_u)
+    gl = np.abs(default().gelu_mul(g, np.ones_like(g)))
+    prop = GELU_LIPSCHITZ * eg * (np.abs(u) + eu) + gl * eu
+    return prop + GELU_EVAL_REL * (gl + GELU_LIPSCHITZ * eg) * (np.abs(u) + eu) + ABS_TOL
+
+
+def check_gate_up(h, g, u, mag_g, mag_u) -> tuple[bool, float, int]:
+    """Accept a gate+up result ``h`` against the oracle's (h_ref = gelu_mul(g, u))."""
+    h = np.asarray(h, dtype=np.float64).reshape(-1)
+    h_ref = default().gelu_mul(g, u).reshape(-1)
+    tol = gate_up_tolerance(g, u, mag_g, mag_u).reshape(-1)
+    if h.size == 0:
+        return True, 0.0, -1
+    err = np.abs(h - h_ref)
+    err = np.where(np.isnan(err), np.inf, err)
+    ratio = err / tol
+    worst = int(np.argmax(ratio))
+    return bool(np.all(err <= tol)), float(ratio[worst]), worst
 
 
 def tolerance(mag: np.ndarray) -> np.ndarray:

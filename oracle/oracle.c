@@ -18,6 +18,8 @@
  *   - bf16 weights are raw u16 bit patterns (oxinfer 0.0.1 src/drafter.rs,
  *     struct `DLayer`: weights held as `&[u16]`); widening to fp32 is the
  *     exact bit shift.
+ *   - gelu_mul after the gate+up batch (oxinfer 0.0.1 src/drafter.rs,
+ *     `Drafter::step`), for the fused gate+up job: at the end of this file.
  *
  * Host byte layout of one weight (one contiguous buffer):
  *   BF16: u16 w[n_out][n_in]
@@ -139,4 +141,22 @@ int oracle_linear_sampled(int format, const void* w, int64_t n_out, int64_t n_in
     mag[s] = m;
   }
   return 0;
+}
+
+/* gelu_mul, the step that follows the shared-input gate+up batch in the pages'
+ * drafter (oxinfer 0.0.1, src/drafter.rs, `Drafter::step`: `matmul_multi` over
+ * gate and up, then `gelu_mul(&mut g, &u)`).  The pages do not print gelu_mul;
+ * the reading taken is g[i] <- gelu(g[i]) * u[i] with gelu in the tanh form of
+ * the Gemma family the pages serve:
+ *   gelu(g) = 0.5 * g * (1 + tanh(sqrt(2/pi) * (g + 0.044715 * g^3))).
+ * Evaluated in double. */
+double oracle_gelu(double g) {
+  const double pi = acos(-1.0);
+  const double inner = sqrt(2.0 / pi) * (g + 0.044715 * g * g * g);
+  return 0.5 * g * (1.0 + tanh(inner));
+}
+
+/* h[i] = gelu(g[i]) * u[i] for i < n (g: gate results, u: up results). */
+void oracle_gelu_mul(const double* g, const double* u, int64_t n, double* h) {
+  for (int64_t i = 0; i < n; ++i) h[i] = oracle_gelu(g[i]) * u[i];
 }

@@ -12,6 +12,7 @@ and ``WeightRef::bytes``; Q8 = int8 with one fp32 scale per 32-block along
 n_in, Q4 = two's-complement nibbles, low nibble first, one fp32 scale per
 32-block, both dequantised as ``fp32(d * q)``.
 """
+import math
 import os
 import shutil
 
@@ -223,10 +224,76 @@ def pin_sampled_matches_definition(orc):
         assert abs(mag[s] - np.abs(prods).sum()) <= 1e-15 * np.abs(prods).sum()
 
 
+# ---------------------------------------------------------------------------
+# gelu_mul after the gate+up batch (oxinfer 0.0.1, src/drafter.rs, Drafter::step;
+# gelu read as the tanh form of the Gemma family)
+# ---------------------------------------------------------------------------
+def _gelu_erf(v):
+    # the exact GELU, v * Phi(v), through the C library's erf (an independent routine)
+    return 0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0)))
+
+
+def pin_gelu_against_erf(orc):
+    # the tanh form stays within 5e-4 of the exact GELU everywhere (max gap ~4.7e-4);
+    # a dropped cubic term (gap 0.033 at 2) or a wrong constant is far outside it
+    for v in np.concatenate([np.linspace(-10.0, 10.0, 2001), [0.5, 1.0, 2.0, -1.0, -3.0]]):
+        assert abs(orc.gelu(float(v)) - _gelu_erf(float(v))) <= 5e-4, v
+
+
+def pin_gelu_identities(orc):
+    # gelu(v) - gelu(-v) = v for the tanh form (tanh is odd); gelu(0) = 0;
+    # gelu(v) -> v for large v and -> 0 for large negative v
+    for v in (0.1, 0.7, 1.5, 3.0, 9.0):
+        assert abs(orc.gelu(v) - orc.gelu(-v) - v) <= 1e-14 * max(1.0, v), v
+    assert orc.gelu(0.0) == 0.0
+    assert orc.gelu(40.0) == 40.0
+    assert orc.gelu(-40.0) == 0.0
+    assert orc.gelu(1.0) > orc.gelu(0.5) > 0.0 > orc.gelu(-0.5)
+
+
+def pin_gelu_lipschitz(orc):
+    # the tolerance of gate+up results assumes sup |gelu'| <= GELU_LIPSCHITZ; the
+    # supremum (about 1.12899 near |v| = 1.4185) must also be close to the constant
+    xs = np.linspace(-6.0, 6.0, 120001)
+    gs = np.array([orc.gelu(float(v)) for v in xs])
+    d = np.diff(gs) / np.diff(xs)
+    assert np.max(np.abs(d)) <= oracle.GELU_LIPSCHITZ
+    assert np.max(np.abs(d)) >= oracle.GELU_LIPSCHITZ - 0.002
+
+
+def pin_gelu_mul_roles(orc):
+    # h = gelu(g) * u: the activation goes on the gate, not on the up result
+    g = np.array([1.0, -3.0, 2.0, 0.0])
+    u = np.array([2.0, 0.5, -3.0, 7.0])
+    h = orc.gelu_mul(g, u)
+    for i in range(4):
+        assert abs(h[i] - _gelu_erf(g[i]) * u[i]) <= 5e-4 * abs(u[i]) + 1e-15, i
+
+
+def pin_gate_up_one_hot(orc):
+    # x = e_k: g and u are column k of the dequantised gate and up weights exactly,
+    # and h = gelu(g) * u
+    n_out, n_in = 24, 64
+    gen = torch.Generator().manual_seed(12)
+    wg = torch.randn(n_out, n_in, generator=gen) * 0.5
+    wu = torch.randn(n_out, n_in, generator=gen) * 0.5
+    for fmt in ("bf16", "q8"):
+        bg, bu = wl.encode_weight(fmt, wg), wl.encode_weight(fmt, wu)
+        dg, du = orc.dequant(fmt, bg, n_out, n_in), orc.dequant(fmt, bu, n_out, n_in)
+        for k in (0, 33, 63):
+            x = np.zeros((1, n_in), dtype=np.float32)
+            x[0, k] = 1.0
+            h, g, u, _, _ = orc.gate_up(fmt, bg, bu, n_out, n_in, x)
+            assert _same_values(g[0], dg[:, k]) and _same_values(u[0], du[:, k]), (fmt, k)
+            ref = np.array([_gelu_erf(float(a)) * float(b) for a, b in zip(dg[:, k], du[:, k])])
+            assert np.all(np.abs(h[0] - ref) <= 5e-4 * np.abs(du[:, k]) + 1e-15), (fmt, k)
+
+
 ALL_PINS = [pin_weight_bytes, pin_bf16_exhaustive, pin_q8_exhaustive, pin_q4_exhaustive,
             pin_block_scale_index, pin_brute_force_small, pin_golden_files, pin_identity,
             pin_one_hot, pin_integer_exact, pin_library_crosscheck,
-            pin_sampled_matches_definition]
+            pin_sampled_matches_definition, pin_gelu_against_erf, pin_gelu_identities,
+            pin_gelu_lipschitz, pin_gelu_mul_roles, pin_gate_up_one_hot]
 
 
 def _read_golden(path):
@@ -303,6 +370,22 @@ def test_check_rule():
     assert not ok
 
 
+def test_gate_up_check_rule():
+    # the derived bound: g and u each off by their full tolerance still pass ...
+    g = np.array([1.4, -2.0, 0.3])
+    u = np.array([2.0, -1.0, 0.0])
+    mag_g = np.array([5.0, 3.0, 1.0])
+    mag_u = np.array([4.0, 2.0, 1.0])
+    eg, eu = oracle.tolerance(mag_g), oracle.tolerance(mag_u)
+    h_worst = oracle.gelu_mul(g + eg, u + eu)
+    assert oracle.check_gate_up(h_worst, g, u, mag_g, mag_u)[0]
+    # ... an error twice the allowance does not, nor does a NaN
+    tol = oracle.gate_up_tolerance(g, u, mag_g, mag_u)
+    ok, _, worst = oracle.check_gate_up(oracle.gelu_mul(g, u) + 2 * tol * np.array([0, 1, 0]), g, u, mag_g, mag_u)
+    assert not ok and worst == 1
+    assert not oracle.check_gate_up([np.nan, 0.0, 0.0], g, u, mag_g, mag_u)[0]
+
+
 def test_oracle_rejects_bad_format(orc):
     with pytest.raises((ValueError, KeyError)):
         orc.dequant(7, np.zeros(64, np.uint8), 1, 32)
@@ -329,6 +412,10 @@ MUTANTS = {
     "bf16_low_half": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b;"),
     "scale_rounded_twice": ("return (float)((double)d * (double)q);",
                             "return (float)(double)(float)((double)(float)d * 1.0000001 * (double)q);"),
+    "gelu_no_cubic": ("(g + 0.044715 * g * g * g)", "(g + 0.0 * g * g * g)"),
+    "gelu_wrong_constant": ("sqrt(2.0 / pi)", "sqrt(pi / 2.0)"),
+    "gelu_sign": ("0.5 * g * (1.0 + tanh(inner))", "0.5 * g * (1.0 - tanh(inner))"),
+    "gelu_mul_roles_swapped": ("h[i] = oracle_gelu(g[i]) * u[i];", "h[i] = oracle_gelu(u[i]) * g[i];"),
 }
 
 
