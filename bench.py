@@ -151,13 +151,20 @@ class Batch:
     def __init__(self, sil, torch, inputs: wl.BatchInputs, copies: int):
         self.inputs = inputs
         self.t, self.n_in = inputs.t, inputs.n_in
-        self.copies = [[sil.upload_weight(f, buf, n, inputs.n_in) for f, buf, n in inputs.jobs]
-                       for _ in range(copies)]
+        if inputs.fused:
+            # one fused gate+up job: h = gelu(g) * u, as wide as one of the two
+            (f, gate, n), (_, up, _) = inputs.jobs
+            self.copies = [[sil.upload_gate_up(f, gate, up, n, inputs.n_in)] for _ in range(copies)]
+            widths = [n]
+        else:
+            self.copies = [[sil.upload_weight(f, buf, n, inputs.n_in) for f, buf, n in inputs.jobs]
+                           for _ in range(copies)]
+            widths = [n for _, _, n in inputs.jobs]
         self.x = torch.from_numpy(inputs.x).cuda()
-        self.ys = [torch.empty((inputs.t, n), device="cuda") for _, _, n in inputs.jobs]
+        self.ys = [torch.empty((inputs.t, n), device="cuda") for n in widths]
         self.weight_bytes = inputs.weight_bytes
         self.flops = inputs.flops
-        self.io_bytes = 4 * inputs.t * inputs.n_in + sum(4 * inputs.t * n for _, _, n in inputs.jobs)
+        self.io_bytes = 4 * inputs.t * inputs.n_in + sum(4 * inputs.t * n for n in widths)
 
     def launch(self, sil, copy: int, stream):
         sil.matmul_batch(self.x, list(zip(self.copies[copy % len(self.copies)], self.ys)),
@@ -299,7 +306,8 @@ def run_per_config(sil, torch, pk, only=None):
                         cache.clear()
                         cache[key] = wl.make_workload_batch(w, bt, t, fmt)
                     base = cache[key]
-                    inp = wl.BatchInputs(fmt, t, bt.n_in, wl.make_x(t, bt.n_in, seed=0), base.jobs)
+                    inp = wl.BatchInputs(fmt, t, bt.n_in, wl.make_x(t, bt.n_in, seed=0), base.jobs,
+                                         fused=base.fused)
                     copies = copies_for(inp.weight_bytes)
                     b = Batch(sil, torch, inp, copies)
                     try:
@@ -330,6 +338,8 @@ def run_per_config(sil, torch, pk, only=None):
                          "n_in": bt.n_in, "n_outs": list(bt.n_outs), "us": round(us, 3),
                          "weight_gbs": round(gbs, 1), "tflops": round(tfl, 3),
                          "weight_bytes": inp.weight_bytes}
+                    if w.fused:
+                        e["fused_gelu_mul"] = True
                     if t <= 8:
                         e["bound"] = "hbm"
                         e["frac_hbm_measured"] = round(gbs / pk["hbm_gbs"], 4)

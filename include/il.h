@@ -75,7 +75,7 @@ typedef struct {
   uint64_t jobs;              /* jobs in those batches                    */
   uint64_t launches;          /* kernels launched by those batches        */
   uint64_t weight_bytes;      /* weight bytes those batches streamed      */
-  uint64_t flops;             /* 2 * t * n_in * n_out summed over jobs    */
+  uint64_t flops;             /* 2 * t * n_in * rows summed over jobs     */
   uint64_t errors;            /* calls that returned an error             */
 } il_stats;
 
@@ -138,6 +138,37 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
 int il_matmul_batch_noalloc(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
                             void* stream);
 
+/*
+ * il_upload_gate_up -- a fused gate+up weight.  The pages run the gate and up
+ * projections as one shared-input batch and pass the two results straight to
+ * gelu_mul (oxinfer 0.0.1, src/drafter.rs, `Drafter::step`: `matmul_multi` over
+ * gate and up, then `gelu_mul(&mut g, &u)`).  A handle made here computes that
+ * pair and the activation in one job:
+ *     h[t][n_out] = gelu(x * Wg^T) * (x * Wu^T)        (elementwise)
+ * with gelu the tanh form of the Gemma family the pages serve,
+ *     gelu(g) = 0.5 * g * (1 + tanh(sqrt(2/pi) * (g + 0.044715 * g^3))).
+ * The pages do not print gelu_mul; this is the reading the library takes.
+ *   format            : il_format of BOTH weights.
+ *   gate_ptr, up_ptr  : HOST pointers, each one weight in the host layout of
+ *                       il_upload_weight with the same n_out and n_in; read
+ *                       during the call only.
+ *   n_out, n_in       : as for il_upload_weight (n_out = width of h).
+ * Returns a handle, or NULL on error.  A job of this handle in il_matmul_batch
+ * (or il_matmul_batch_noalloc) takes n_out = the width of h and y = h
+ * [t][n_out]; it can share a batch with plain jobs.  Inside, the two weights
+ * are stored as one matrix of 2*n_out rows, row 2r = gate row r and row 2r+1 =
+ * up row r, so every kernel finds a pair in adjacent rows.  il_weight_bytes
+ * gives the sum of both weights' bytes; il_weight_info the format, n_out (the
+ * width of h) and n_in; il_dequantize_weight writes the interleaved
+ * [2*n_out][n_in] matrix.
+ */
+il_weight* il_upload_gate_up(int format, const void* gate_ptr, const void* up_ptr, int64_t n_out,
+                             int64_t n_in);
+
+/* 1 if the handle came from il_upload_gate_up, 0 if from il_upload_weight,
+ * -1 for an invalid handle. */
+int il_weight_is_gate_up(const il_weight* w);
+
 /* Releases a handle and its device memory (synchronises the device).
  * NULL is ignored; an unknown pointer is ignored and counted as an error. */
 void il_free_weight(il_weight* w);
@@ -147,7 +178,8 @@ void il_free_weight(il_weight* w);
  * invalid handle. */
 int64_t il_weight_bytes(const il_weight* w);
 
-/* Format and shape of a handle.  Any out pointer may be NULL. */
+/* Format and shape of a handle (for a gate+up handle, n_out is the width of
+ * h).  Any out pointer may be NULL. */
 int il_weight_info(const il_weight* w, int* format, int64_t* n_out, int64_t* n_in);
 
 /*
@@ -155,7 +187,8 @@ int il_weight_info(const il_weight* w, int* format, int64_t* n_out, int64_t* n_i
  * weight as fp32 to dev_out [n_out][n_in] (DEVICE pointer, 4-byte aligned),
  * reading the packed device layout with the same element decoders the matmul
  * kernels use.  bf16 widens exactly; Q8/Q4 give fp32(d*q).  Asynchronous on
- * `stream`.
+ * `stream`.  For a gate+up handle dev_out is [2*n_out][n_in], rows interleaved
+ * as described at il_upload_gate_up.
  */
 int il_dequantize_weight(const il_weight* w, float* dev_out, void* stream);
 

@@ -77,6 +77,10 @@ def load() -> ctypes.CDLL:
         lib.il_matmul_batch.restype = ci
         lib.il_matmul_batch_noalloc.argtypes = [vp, i64, i64, ctypes.POINTER(_Job), ci, vp]
         lib.il_matmul_batch_noalloc.restype = ci
+        lib.il_upload_gate_up.argtypes = [ci, vp, vp, i64, i64]
+        lib.il_upload_gate_up.restype = vp
+        lib.il_weight_is_gate_up.argtypes = [vp]
+        lib.il_weight_is_gate_up.restype = ci
         lib.il_free_weight.argtypes = [vp]
         lib.il_free_weight.restype = None
         lib.il_weight_bytes.argtypes = [vp]
@@ -119,11 +123,12 @@ def version() -> int:
 class Weight:
     """Owner of one device weight handle (freed on :meth:`free` or garbage collection)."""
 
-    def __init__(self, handle: int, fmt: int, n_out: int, n_in: int):
+    def __init__(self, handle: int, fmt: int, n_out: int, n_in: int, gate_up: bool = False):
         self.handle = handle
         self.fmt = fmt
-        self.n_out = n_out
+        self.n_out = n_out      # columns of a job's output (the width of h for gate+up)
         self.n_in = n_in
+        self.gate_up = gate_up
 
     @property
     def bytes(self) -> int:
@@ -153,6 +158,24 @@ def upload_weight(fmt, host, n_out: int, n_in: int) -> Weight:
     if not h:
         raise ILError(lib.il_last_status(), last_error())
     return Weight(h, _fmt(fmt), int(n_out), int(n_in))
+
+
+def upload_gate_up(fmt, gate, up, n_out: int, n_in: int) -> Weight:
+    """``il_upload_gate_up``: ``gate`` and ``up`` are host buffers of one shape in the
+    layout of :func:`upload_weight`; a job of the result writes ``h = gelu(g) * u``,
+    ``[t][n_out]``."""
+    g = np.ascontiguousarray(gate)
+    u = np.ascontiguousarray(up)
+    lib = load()
+    h = lib.il_upload_gate_up(_fmt(fmt), g.ctypes.data, u.ctypes.data, int(n_out), int(n_in))
+    if not h:
+        raise ILError(lib.il_last_status(), last_error())
+    return Weight(h, _fmt(fmt), int(n_out), int(n_in), gate_up=True)
+
+
+def is_gate_up(w) -> int:
+    """``il_weight_is_gate_up``: 1, 0, or -1 for an invalid handle."""
+    return int(load().il_weight_is_gate_up(w.handle if isinstance(w, Weight) else w))
 
 
 def free_weight(w: Weight) -> None:
@@ -213,7 +236,8 @@ def matmul_batch(x, jobs, stream=None) -> None:
 
 
 def dequantize_weight(w: Weight, out, stream=None) -> None:
-    """Test hook: every element of ``w`` as fp32 into ``out`` ([n_out][n_in], CUDA)."""
+    """Test hook: every element of ``w`` as fp32 into ``out`` ([n_out][n_in], CUDA;
+    [2*n_out][n_in] with gate/up rows interleaved for a gate+up weight)."""
     _check(load().il_dequantize_weight(w.handle, out.data_ptr(), _stream_ptr(stream)))
 
 

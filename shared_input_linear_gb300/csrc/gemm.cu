@@ -53,6 +53,7 @@ struct __align__(64) GemmParams {
   unsigned* counters;  // split-K arrivals per tile, zero before the launch
   int stall_producer;  // failure-detection test: the producer never loads, so the MMA wait runs out
   unsigned* status;
+  unsigned glu_mask;   // bit j: job j's rows interleave gate/up; y[j] is h = gelu(g) * u, n_out/2 wide
 };
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -321,6 +322,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
       locate_tile(p, tile, job, mt, nt);
       const int n_out = p.n_out[job];
       float* y = p.y[job];
+      const bool glu = (p.glu_mask >> job) & 1u;  // uniform over the CTA
       const int lrow = quarter * 32 + lane;
       const int row = mt * kBM + lrow;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
@@ -333,6 +335,21 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
           // partial tile stored [token][row]: each store of the warp is 128 contiguous bytes
 #pragma unroll
           for (int j = 0; j < 32; ++j) part[(c0 + j) * kBM + lrow] = __uint_as_float(r[j]);
+        } else if (glu) {
+          // lanes 2i (gate) and 2i+1 (up) hold output column row / 2 for 32 tokens and
+          // split them: the even lane finishes tokens 0..15, the odd lane 16..31, each
+          // trading the other half with its partner.  n_out is even, so a pair is
+          // either wholly inside or wholly outside the weight.
+          const bool odd = lane & 1;
+          const int tok0 = nt * BN + c0 + (odd ? 16 : 0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float keep = __uint_as_float(odd ? r[j + 16] : r[j]);
+            const float got = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? r[j] : r[j + 16]), 1);
+            const int tok = tok0 + j;
+            if (row < n_out && tok < p.t)
+              y[(int64_t)tok * (n_out >> 1) + (row >> 1)] = odd ? gelu_mul(got, keep) : gelu_mul(keep, got);
+          }
         } else {
           const int tok0 = nt * BN + c0;
           if (row < n_out) {
@@ -361,12 +378,15 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
           *last_flag = last;
         }
         epi_bar();
-        if (*last_flag && row < n_out) {
+        // *last_flag is the same for the whole CTA, so the warps stay converged for
+        // the gate/up exchange below
+        if (*last_flag && (glu || row < n_out)) {
           const float* base = p.ws + (size_t)tile * p.splits * (BN * kBM) + lrow;
           const int ntok = min(BN, p.t - nt * BN);
 #pragma unroll 1
           for (int c0 = 0; c0 < ntok; c0 += 16) {
             // 16 tokens at a time: independent loads in flight, slices summed in order
+            // (a partial tile holds every token column, so reads past ntok stay inside it)
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
@@ -376,9 +396,22 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + j * kBM);
             }
+            if (glu) {
+              // as in the direct store: the even lane finishes tokens 0..7, the odd 8..15
+              const bool odd = lane & 1;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < ntok) y[(int64_t)(nt * BN + c0 + j) * n_out + row] = v[j];
+              for (int j = 0; j < 8; ++j) {
+                const float keep = odd ? v[j + 8] : v[j];
+                const float got = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + 8], 1);
+                const int c = c0 + j + (odd ? 8 : 0);
+                if (row < n_out && c < ntok)
+                  y[(int64_t)(nt * BN + c) * (n_out >> 1) + (row >> 1)] = odd ? gelu_mul(got, keep) : gelu_mul(keep, got);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < ntok) y[(int64_t)(nt * BN + c0 + j) * n_out + row] = v[j];
+            }
           }
         }
       }
@@ -589,6 +622,7 @@ cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
         return cudaErrorInvalidValue;
       p.y[j] = jobs[j0 + j].y;
       p.n_out[j] = (int)w.n_out;
+      if (w.glu) p.glu_mask |= 1u << j;
       p.tile_begin[j] = tiles;
       tiles += (int)((w.n_out + kBM - 1) / kBM) * p.n_tiles_n;
     }

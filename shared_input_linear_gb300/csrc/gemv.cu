@@ -183,12 +183,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
       k = F::CK * c_begin + 16 * s + 4 * qq;
     return m < p.t && k < p.n_in && s < c_cnt * F::SPC;
   };
-  // Q8/Q4 (fp16 path): scale x by 2^-x_exp so that the slice's largest |x| lies in
-  // [2^13, 2^14), well inside fp16's range; the epilogue multiplies by 2^x_exp.
+  // Q8/Q4 (fp16 path): scale each token's x by 2^-x_exp so that its largest |x| in
+  // this slice lies in [2^13, 2^14), well inside fp16's range; the epilogue
+  // multiplies by 2^x_exp.  The scale is per token, so a token's precision does not
+  // depend on the magnitudes of the others.  x_exp stays in [-126, 114]: both powers
+  // of two are normal floats and even |x| near FLT_MAX (ilogb 127) lands in range.
+  // A thread's staging elements e all have e % 32 == lane, so it only ever sees
+  // token n = lane / 4: the max reduces over the four lanes q of that token.
   int x_exp = 0;
   if (FMT != IL_BF16) {
-    __shared__ unsigned s_max_bits;
-    if (threadIdx.x == 0) s_max_bits = 0u;
+    __shared__ unsigned s_max_bits[8];
+    if (threadIdx.x < 8) s_max_bits[threadIdx.x] = 0u;
     __syncthreads();
     float mx = 0.f;
     for (int e = threadIdx.x; e < slots * 32; e += kThreads) {
@@ -198,12 +203,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
         mx = fmaxf(mx, fmaxf(fmaxf(fabsf(xv.x), fabsf(xv.y)), fmaxf(fabsf(xv.z), fabsf(xv.w))));
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0 && mx > 0.f) atomicMax(&s_max_bits, __float_as_uint(mx));  // non-negative: bits order as values
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (q == 0 && mx > 0.f) atomicMax(&s_max_bits[n], __float_as_uint(mx));  // non-negative: bits order as values
     __syncthreads();
-    const float smax = __uint_as_float(s_max_bits);
-    x_exp = smax > 0.f ? max(-110, min(110, ilogbf(smax) - 13)) : 0;
+    const float smax = __uint_as_float(s_max_bits[n]);
+    x_exp = smax > 0.f ? max(-126, min(114, ilogbf(smax) - 13)) : 0;
   }
   const float x_scale = ldexpf(1.0f, -x_exp);
   for (int e = threadIdx.x; e < slots * 32; e += kThreads) {
@@ -253,9 +258,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
         if (gidx < p.total_groups && n < p.t) {
           const DecodeJob& jb = p.jobs[find_job(p, gidx)];
           const int row0 = (gidx - jb.group_begin) * 8 + 2 * q;
-          float* y = jb.y + (int64_t)n * jb.n_out + row0;
-          if (row0 < jb.n_out) y[0] = v[g][0];
-          if (row0 + 1 < jb.n_out) y[1] = v[g][1];
+          if (jb.glu) {
+            // rows 2q, 2q+1 are gate and up of output column row0 / 2
+            if (row0 < jb.n_out) jb.y[(int64_t)n * (jb.n_out >> 1) + (row0 >> 1)] = gelu_mul(v[g][0], v[g][1]);
+          } else {
+            float* y = jb.y + (int64_t)n * jb.n_out + row0;
+            if (row0 < jb.n_out) y[0] = v[g][0];
+            if (row0 + 1 < jb.n_out) y[1] = v[g][1];
+          }
         }
       }
     } else {
@@ -265,17 +275,28 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
         *reinterpret_cast<float2*>(rbuf + (warp * G + g) * 64 + n * 8 + 2 * q) = make_float2(v[g][0], v[g][1]);
       cg::cluster_group cluster = cg::this_cluster();
       cluster.sync();
-      const int per = (GPB * 64 + p.slices - 1) / p.slices;
-      const int e_end = min(GPB * 64, (rank + 1) * per);
+      // each rank sums (over the slices, in rank order) and stores its share of
+      // the row block, one pair of adjacent rows (2i, 2i+1) at a time
+      const int per = (GPB * 32 + p.slices - 1) / p.slices;
+      const int e_end = min(GPB * 32, (rank + 1) * per);
       for (int e = rank * per + threadIdx.x; e < e_end; e += kThreads) {
-        const int gl = e >> 6, m = (e >> 3) & 7, r = e & 7;
+        const int gl = e >> 5, m = (e >> 2) & 7, r = 2 * (e & 3);
         const int gidx = rb * GPB + gl;
         if (gidx < p.total_groups && m < p.t) {
-          float s = 0.f;
-          for (int src = 0; src < p.slices; ++src) s += cluster.map_shared_rank(rbuf, src)[e];
+          float2 s = make_float2(0.f, 0.f);
+          for (int src = 0; src < p.slices; ++src) {
+            const float2 v2 = reinterpret_cast<const float2*>(cluster.map_shared_rank(rbuf, src))[e];
+            s.x += v2.x;
+            s.y += v2.y;
+          }
           const DecodeJob& jb = p.jobs[find_job(p, gidx)];
           const int row = (gidx - jb.group_begin) * 8 + r;
-          if (row < jb.n_out) jb.y[(int64_t)m * jb.n_out + row] = s;
+          if (jb.glu) {
+            if (row < jb.n_out) jb.y[(int64_t)m * (jb.n_out >> 1) + (row >> 1)] = gelu_mul(s.x, s.y);
+          } else {
+            if (row < jb.n_out) jb.y[(int64_t)m * jb.n_out + row] = s.x;
+            if (row + 1 < jb.n_out) jb.y[(int64_t)m * jb.n_out + row + 1] = s.y;
+          }
         }
       }
     }

@@ -257,27 +257,35 @@ void il_reset_stats(void) {
   g_stats.errors = 0;
 }
 
-il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int64_t n_in) {
+}  // extern "C"
+
+namespace {
+
+// Shared by il_upload_weight (parts = 1) and il_upload_gate_up (parts = 2): the
+// parts, host weights of one shape, become one packed matrix whose rows
+// interleave them (row parts*r + i is row r of part i).
+il_weight* upload_impl(const char* fn, int format, const void* const* host, int parts, int64_t n_out,
+                       int64_t n_in) {
   clear_error();
   if (format != IL_BF16 && format != IL_Q8 && format != IL_Q4) {
-    fail(IL_ERR_FORMAT, "il_upload_weight: unknown format %d", format);
+    fail(IL_ERR_FORMAT, "%s: unknown format %d", fn, format);
     return nullptr;
   }
-  if (host_ptr == nullptr) {
-    fail(IL_ERR_ARG, "il_upload_weight: host_ptr is NULL");
-    return nullptr;
-  }
-  if (n_out < 1 || n_out > kMaxNOut || n_in < 1 || n_in > kMaxNIn) {
-    fail(IL_ERR_SHAPE, "il_upload_weight: n_out=%lld n_in=%lld out of range", (long long)n_out,
-         (long long)n_in);
+  for (int i = 0; i < parts; ++i)
+    if (host[i] == nullptr) {
+      fail(IL_ERR_ARG, "%s: host pointer %d is NULL", fn, i);
+      return nullptr;
+    }
+  if (n_out < 1 || n_out > kMaxNOut / parts || n_in < 1 || n_in > kMaxNIn) {
+    fail(IL_ERR_SHAPE, "%s: n_out=%lld n_in=%lld out of range", fn, (long long)n_out, (long long)n_in);
     return nullptr;
   }
   if (format == IL_BF16 && n_in % 8 != 0) {
-    fail(IL_ERR_SHAPE, "il_upload_weight: bf16 needs n_in %% 8 == 0 (got %lld)", (long long)n_in);
+    fail(IL_ERR_SHAPE, "%s: bf16 needs n_in %% 8 == 0 (got %lld)", fn, (long long)n_in);
     return nullptr;
   }
   if (format != IL_BF16 && n_in % 32 != 0) {
-    fail(IL_ERR_SHAPE, "il_upload_weight: Q8/Q4 need n_in %% 32 == 0 (got %lld)", (long long)n_in);
+    fail(IL_ERR_SHAPE, "%s: Q8/Q4 need n_in %% 32 == 0 (got %lld)", fn, (long long)n_in);
     return nullptr;
   }
   DeviceState* ds = nullptr;
@@ -286,19 +294,21 @@ il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int
 
   PackedWeight* w = new (std::nothrow) PackedWeight();
   if (w == nullptr) {
-    fail(IL_ERR_OOM, "il_upload_weight: host allocation failed");
+    fail(IL_ERR_OOM, "%s: host allocation failed", fn);
     return nullptr;
   }
+  const int64_t rows = n_out * parts;
   w->magic = kWeightMagic;
   w->format = format;
   w->device = dev;
-  w->n_out = n_out;
+  w->glu = parts == 2 ? 1 : 0;
+  w->n_out = rows;
   w->n_in = n_in;
-  w->n_out_pad = (n_out + kGroupRows - 1) / kGroupRows * kGroupRows;
+  w->n_out_pad = (rows + kGroupRows - 1) / kGroupRows * kGroupRows;
   w->n_in_pad = (n_in + kPadK - 1) / kPadK * kPadK;
   w->n_groups = w->n_out_pad / kGroupRows;
   w->n_chunks = w->n_in_pad / chunk_k(format);
-  w->host_bytes = host_bytes(format, n_out, n_in);
+  w->host_bytes = host_bytes(format, rows, n_in);
   size_t qbytes = format == IL_BF16 ? (size_t)w->n_out_pad * w->n_in_pad * 2
                                     : (size_t)w->n_groups * w->n_chunks * kChunkBytes;
   size_t sbytes = format == IL_BF16 ? 0 : (size_t)w->n_groups * w->n_chunks * chunk_scale_bytes(format);
@@ -311,7 +321,7 @@ il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int
     cudaGetLastError();
     const size_t want = w->device_bytes;
     delete w;
-    fail(IL_ERR_OOM, "il_upload_weight: cudaMalloc(%zu) failed", want);
+    fail(IL_ERR_OOM, "%s: cudaMalloc(%zu) failed", fn, want);
     return nullptr;
   }
   w->quants = static_cast<uint8_t*>(mem);
@@ -324,17 +334,32 @@ il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int
     cudaFree(mem);
     const long long want = (long long)w->host_bytes;
     delete w;
-    fail(IL_ERR_OOM, "il_upload_weight: staging cudaMalloc(%lld) failed", want);
+    fail(IL_ERR_OOM, "%s: staging cudaMalloc(%lld) failed", fn, want);
     return nullptr;
   }
-  e = cudaMemcpy(staging, host_ptr, (size_t)w->host_bytes, cudaMemcpyHostToDevice);
+  if (parts == 1) {
+    e = cudaMemcpy(staging, host[0], (size_t)w->host_bytes, cudaMemcpyHostToDevice);
+  } else {
+    // host layout of each part: [n_out rows of qrow bytes][n_out rows of srow bytes];
+    // pitched copies put part i's rows at every parts-th row of the staging copy
+    const size_t qrow = (size_t)host_bytes(format, 1, n_in) - (format == IL_BF16 ? 0 : 4 * (size_t)(n_in / 32));
+    const size_t srow = format == IL_BF16 ? 0 : 4 * (size_t)(n_in / 32);
+    uint8_t* st = static_cast<uint8_t*>(staging);
+    for (int i = 0; i < parts && e == cudaSuccess; ++i) {
+      const uint8_t* src = static_cast<const uint8_t*>(host[i]);
+      e = cudaMemcpy2D(st + i * qrow, parts * qrow, src, qrow, qrow, (size_t)n_out, cudaMemcpyHostToDevice);
+      if (e == cudaSuccess && srow > 0)
+        e = cudaMemcpy2D(st + (size_t)rows * qrow + i * srow, parts * srow, src + (size_t)n_out * qrow, srow, srow,
+                         (size_t)n_out, cudaMemcpyHostToDevice);
+    }
+  }
   if (e == cudaSuccess) e = launch_pack(*w, static_cast<const uint8_t*>(staging), 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(0);
   cudaFree(staging);
   if (e != cudaSuccess) {
     cudaFree(mem);
     delete w;
-    cuda_fail(e, "il_upload_weight: copy/pack");
+    cuda_fail(e, "upload: copy/pack");
     return nullptr;
   }
   {
@@ -344,6 +369,25 @@ il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int
   g_stats.uploads.fetch_add(1);
   g_stats.upload_bytes.fetch_add((uint64_t)w->host_bytes);
   return reinterpret_cast<il_weight*>(w);
+}
+
+}  // namespace
+
+extern "C" {
+
+il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int64_t n_in) {
+  const void* host[1] = {host_ptr};
+  return upload_impl("il_upload_weight", format, host, 1, n_out, n_in);
+}
+
+il_weight* il_upload_gate_up(int format, const void* gate_ptr, const void* up_ptr, int64_t n_out, int64_t n_in) {
+  const void* host[2] = {gate_ptr, up_ptr};
+  return upload_impl("il_upload_gate_up", format, host, 2, n_out, n_in);
+}
+
+int il_weight_is_gate_up(const il_weight* h) {
+  if (h == nullptr || !known_handle(h)) return -1;
+  return reinterpret_cast<const PackedWeight*>(h)->glu;
 }
 
 void il_free_weight(il_weight* h) {
@@ -374,7 +418,7 @@ int il_weight_info(const il_weight* h, int* format, int64_t* n_out, int64_t* n_i
   if (h == nullptr || !known_handle(h)) return fail(IL_ERR_HANDLE, "il_weight_info: invalid handle");
   const PackedWeight* w = reinterpret_cast<const PackedWeight*>(h);
   if (format) *format = w->format;
-  if (n_out) *n_out = w->n_out;
+  if (n_out) *n_out = out_width(*w);
   if (n_in) *n_in = w->n_in;
   return IL_OK;
 }
@@ -456,14 +500,14 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
       if (w->n_in != n_in)
         return fail(IL_ERR_SHAPE, "il_matmul_batch: job %d weight n_in=%lld, batch n_in=%lld", j,
                     (long long)w->n_in, (long long)n_in);
-      if (jobs[j].n_out != w->n_out)
+      if (jobs[j].n_out != out_width(*w))
         return fail(IL_ERR_SHAPE, "il_matmul_batch: job %d n_out=%lld, weight n_out=%lld", j,
-                    (long long)jobs[j].n_out, (long long)w->n_out);
+                    (long long)jobs[j].n_out, (long long)out_width(*w));
       if (jobs[j].y == nullptr) return fail(IL_ERR_ARG, "il_matmul_batch: job %d y is NULL", j);
       if (reinterpret_cast<uintptr_t>(jobs[j].y) % 4 != 0)
         return fail(IL_ERR_ARG, "il_matmul_batch: job %d y is not 4-byte aligned", j);
       const uintptr_t y0 = reinterpret_cast<uintptr_t>(jobs[j].y);
-      ranges.emplace_back(y0, y0 + (uintptr_t)(t * w->n_out * 4));
+      ranges.emplace_back(y0, y0 + (uintptr_t)(t * out_width(*w) * 4));
       wbytes += (uint64_t)w->host_bytes;
       flops += 2ull * (uint64_t)t * (uint64_t)n_in * (uint64_t)w->n_out;
     }
@@ -554,8 +598,9 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
           DecodeJob& dj = p.jobs[p.n_jobs++];
           dj.w = w->quants;
           dj.s = w->scales;
-          dj.y = jobs[idx[j]].y + t0 * w->n_out;
+          dj.y = jobs[idx[j]].y + t0 * out_width(*w);
           dj.n_out = (int32_t)w->n_out;
+          dj.glu = w->glu;
           dj.group_begin = groups;
           dj.row_stride = fmt == IL_BF16 ? w->n_in_pad : w->n_chunks;
           groups += (int)w->n_groups;
@@ -614,12 +659,12 @@ int api_check_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
       if (w->device != dev) return fail(IL_ERR_HANDLE, "job %d weight lives on device %d", j, w->device);
       if (w->n_in != n_in) return fail(IL_ERR_SHAPE, "job %d weight n_in=%lld, batch n_in=%lld", j,
                                        (long long)w->n_in, (long long)n_in);
-      if (jobs[j].n_out != w->n_out) return fail(IL_ERR_SHAPE, "job %d n_out=%lld, weight n_out=%lld", j,
-                                                 (long long)jobs[j].n_out, (long long)w->n_out);
+      if (jobs[j].n_out != out_width(*w)) return fail(IL_ERR_SHAPE, "job %d n_out=%lld, weight n_out=%lld", j,
+                                                      (long long)jobs[j].n_out, (long long)out_width(*w));
       if (jobs[j].y == nullptr) return fail(IL_ERR_ARG, "job %d y is NULL", j);
       if (reinterpret_cast<uintptr_t>(jobs[j].y) % 4 != 0) return fail(IL_ERR_ARG, "job %d y is not 4-byte aligned", j);
       const uintptr_t y0 = reinterpret_cast<uintptr_t>(jobs[j].y);
-      ranges.emplace_back(y0, y0 + (uintptr_t)(t * w->n_out * 4));
+      ranges.emplace_back(y0, y0 + (uintptr_t)(t * out_width(*w) * 4));
       ws->push_back(w);
       *wbytes += (uint64_t)w->host_bytes;
       *flops += 2ull * (uint64_t)t * (uint64_t)n_in * (uint64_t)w->n_out;

@@ -38,11 +38,15 @@ __host__ __device__ constexpr int blocks_per_chunk(int fmt) { return fmt == IL_Q
 // Scale bytes per (group, chunk): 8 rows x blocks x 4 bytes.
 __host__ __device__ constexpr int chunk_scale_bytes(int fmt) { return 32 * blocks_per_chunk(fmt); }
 
+// A gate+up weight (il_upload_gate_up) is stored as one matrix of n_out = 2*width
+// rows, row 2r = gate row r and row 2r+1 = up row r; its jobs write
+// h = gelu(gate) * up, `width` columns wide.
 struct PackedWeight {
   uint64_t magic;
   int format;
   int device;
-  int64_t n_out, n_in;
+  int glu;                     // 1: rows interleaved gate/up, output h = gelu(g) * u
+  int64_t n_out, n_in;         // n_out: packed rows (2 * width of h for glu)
   int64_t n_out_pad, n_in_pad;
   int64_t n_groups, n_chunks;  // n_out_pad / 8, n_in_pad / chunk_k
   uint8_t* quants;             // device, packed as above
@@ -52,6 +56,9 @@ struct PackedWeight {
 };
 constexpr uint64_t kWeightMagic = 0x696c5f7765696768ull;  // "il_weigh"
 
+// Columns of a job's output: n_out, or n_out / 2 for a gate+up weight.
+inline int64_t out_width(const PackedWeight& w) { return w.glu ? w.n_out / 2 : w.n_out; }
+
 // ---------------------------------------------------------------------------
 // Decode (t <= 8) job table, passed by value as a kernel parameter
 // ---------------------------------------------------------------------------
@@ -60,10 +67,12 @@ constexpr int kMaxDecodeJobs = 32;
 struct DecodeJob {
   const uint8_t* w;      // packed quants / bf16
   const float* s;        // packed scales (Q8/Q4)
-  float* y;              // [t][n_out]
-  int32_t n_out;
+  float* y;              // [t][n_out], or h [t][n_out / 2] when glu
+  int32_t n_out;         // packed rows
   int32_t group_begin;   // first global group index of this job
   int64_t row_stride;    // bf16: n_in_pad (elements); Q: n_chunks (chunks per group)
+  int32_t glu;           // rows interleaved gate/up: store gelu(g) * u
+  int32_t pad_;
 };
 
 struct DecodeParams {
@@ -143,6 +152,18 @@ __device__ __forceinline__ float f16_hi(uint32_t v) { return __half2float(__usho
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// gelu in the tanh form used by the Gemma family (the model the pages' drafter
+// belongs to): 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))).  Applied to the
+// fp32 gate result, then multiplied by the fp32 up result.
+// Since 1 + tanh(z) = 2 / (1 + e^(-2z)), gelu(g) = g / (1 + e^(-2z)): one
+// exponential and one fast division instead of a tanh.  The exponent is capped
+// at 88 (e^88 ~ 1.7e38 is still finite); there the quotient is 0 to fp32, which
+// is gelu's limit.
+__device__ __forceinline__ float gelu_mul(float g, float u) {
+  const float z = 0.7978845608028654f * fmaf(0.044715f * g, g * g, g);
+  return __fdividef(g, 1.0f + __expf(fminf(-2.0f * z, 88.0f))) * u;
+}
+
 // ---------------------------------------------------------------------------
 // Launchers (each returns a cudaError_t; the API layer maps it to il_status)
 // ---------------------------------------------------------------------------
@@ -158,7 +179,7 @@ cudaError_t launch_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_
 
 struct GemmJob {
   const PackedWeight* w;
-  float* y;
+  float* y;  // [t][w->n_out], or h [t][w->n_out / 2] when w->glu
 };
 // Tensor-core path for large t (bf16 weights): xb is x cast to bf16,
 // [t][n_in_pad], zero in the padding columns.

@@ -139,8 +139,9 @@ extern "C" int il_matmul_batch_noalloc(const float* x, int64_t t, int64_t n_in, 
           DecodeJob& dj = p.jobs[p.n_jobs++];
           dj.w = w->quants;
           dj.s = w->scales;
-          dj.y = jobs[idx[j]].y + t0 * w->n_out;
+          dj.y = jobs[idx[j]].y + t0 * out_width(*w);
           dj.n_out = (int32_t)w->n_out;
+          dj.glu = w->glu;
           dj.group_begin = groups;
           dj.row_stride = fmt == IL_BF16 ? w->n_in_pad : w->n_chunks;
           groups += (int)w->n_groups;

@@ -166,6 +166,27 @@ def test_one_hot_exact(sil, fmt, t_total):
         assert np.array_equal(y, deq[:, ks].T.astype(np.float32)), f
 
 
+TOKEN_SCALES = (1e36, 1.0, 1e-30, 0.0, 1e-42, 3e-5, 2e20, 1e-12)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+@pytest.mark.parametrize("t", [4, 8, 24])
+def test_extreme_token_magnitudes(sil, fmt, t):
+    # tokens of one batch whose magnitudes differ by up to 10^78 (plus an all-zero token
+    # and a subnormal one): each token must meet the bar on its own, so no token's
+    # precision may depend on the others' range
+    n_in, n_outs = 512, (136, 40)
+    b = wl.make_batch(n_in, n_outs, t, fmt, seed=21)
+    scales = np.array([TOKEN_SCALES[i % len(TOKEN_SCALES)] for i in range(t)], dtype=np.float64)
+    x = (b.x.astype(np.float64) * scales[:, None]).astype(np.float32)
+    bb = wl.BatchInputs(fmt, t, n_in, x, b.jobs)
+    ys, guards = run(sil, bb)
+    assert guards
+    for y in ys:
+        assert np.all(np.isfinite(y))
+    assert_parity(bb, ys, "extreme tokens")
+
+
 @pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
 @pytest.mark.parametrize("t", [1, 8, 40])
 def test_integer_exact(sil, fmt, t):

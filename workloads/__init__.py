@@ -51,6 +51,7 @@ class Workload:
     ts: tuple
     batches: tuple
     note: str = ""
+    fused: bool = False   # each batch's two jobs run as one fused gate+up job (h = gelu(g) * u)
 
 
 TINY = Workload("tiny_bf16", ("bf16",), (1, 4),
@@ -77,7 +78,11 @@ VOCAB = Workload("vocab_projection", ("bf16", "q4"), (1, 8),
                  (Batch("vocab", 2560, (262144,)),),
                  "one very tall job")
 
-WORKLOADS = (TINY, DECODE_BF16, DECODE_QUANT, PREFILL_BF16, VOCAB, PREFILL_QUANT)
+GATE_UP_FUSED = Workload("gate_up_fused", ("bf16", "q8", "q4"), (1, 8, 512),
+                         (Batch("gate_up", 4096, (12288, 12288)),),
+                         "gate+up as one fused job writing h = gelu(g) * u", fused=True)
+
+WORKLOADS = (TINY, DECODE_BF16, DECODE_QUANT, PREFILL_BF16, VOCAB, PREFILL_QUANT, GATE_UP_FUSED)
 BY_NAME = {w.name: w for w in WORKLOADS}
 
 
@@ -165,6 +170,7 @@ class BatchInputs:
     n_in: int
     x: np.ndarray                      # fp32 [t][n_in]
     jobs: list = field(default_factory=list)   # [(fmt, host_bytes u8, n_out)]
+    fused: bool = False                # jobs are (gate, up) of one fused gate+up job
 
     @property
     def weight_bytes(self) -> int:
@@ -190,7 +196,9 @@ def make_batch(n_in: int, n_outs, t: int, fmt: str, seed: int = 0,
 def make_workload_batch(workload: Workload, batch: Batch, t: int, fmt: str,
                         seed: int = 0) -> BatchInputs:
     assert fmt in workload.fmts and t in workload.ts
-    return make_batch(batch.n_in, batch.n_outs, t, fmt, seed)
+    b = make_batch(batch.n_in, batch.n_outs, t, fmt, seed)
+    b.fused = workload.fused
+    return b
 
 
 def make_x(t: int, n_in: int, seed: int) -> np.ndarray:
