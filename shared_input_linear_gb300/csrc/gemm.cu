@@ -15,11 +15,18 @@
 //
 // Warp roles (6 warps): 0 = TMA producer, 1 = TMEM allocator + MMA issuer,
 // 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+//
+// Q8 / Q4 weights (a mixed-input GEMM, 10 warps): the producer brings the packed
+// quants and scales of 16 row groups (128 rows) x one chunk by TMA into a ring of
+// raw stages; warps 6..9 turn them into the bf16 A tile of a pipeline stage,
+// bf16(fp32(d*q)) with round to nearest even, written in the 128-byte swizzle
+// the MMA reads.  The weight crosses HBM once, in its packed form.
 // Every mbarrier wait is bounded; a wait that gives up records an error code
 // in the device status word, raises a CTA-wide abort flag and lets every role
 // leave its loop; TMEM is always released before exit.
 #include <cuda.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 
@@ -31,13 +38,23 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBK = 64;            // bf16 columns per stage: one 128-byte swizzle row
 constexpr int kStages = 4;
-constexpr int kThreadsGemm = 192;  // 6 warps
+constexpr int kThreadsGemm = 192;  // 6 warps (bf16 weights)
+constexpr int kXfWarps = 16;       // Q8/Q4: warps that dequantise raw stages into A tiles
+constexpr int kThreadsQ = kThreadsGemm + 32 * kXfWarps;
+constexpr int kRawStages = 3;
+constexpr uint32_t kRawQuantBytes = 16 * 512;   // one chunk of 16 row groups
+constexpr uint32_t kRawStageBytes = kRawQuantBytes + 16 * 8 * 4 * 4;  // + scales (Q4: 4 blocks a chunk)
+
+__host__ __device__ constexpr int gemm_threads(int fmt) { return fmt == IL_BF16 ? kThreadsGemm : kThreadsQ; }
+// fp32 scales per (row group, chunk): 8 rows x the chunk's 32-blocks
+__host__ __device__ constexpr int scales_per_chunk(int fmt) { return 8 * blocks_per_chunk(fmt); }
 constexpr unsigned long long kWaitLimitCycles = 2ull << 30;  // ~1 s at 2 GHz
 
 constexpr int kMaxGemmJobs = 8;
 
 struct __align__(64) GemmParams {
-  CUtensorMap wmap[kMaxGemmJobs];
+  CUtensorMap wmap[kMaxGemmJobs];  // bf16: W tiles; Q8/Q4: packed quants, [n_groups][n_chunks * 128] words
+  CUtensorMap smap[kMaxGemmJobs];  // Q8/Q4: packed scales, [n_groups][n_chunks * scales_per_chunk] floats
   CUtensorMap xmap;
   float* y[kMaxGemmJobs];
   int n_out[kMaxGemmJobs];
@@ -192,22 +209,77 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: 
 constexpr unsigned kStProducer = 0x1;
 constexpr unsigned kStMma = 0x2;
 constexpr unsigned kStEpilogue = 0x4;
+constexpr unsigned kStTransform = 0x8;
 
-template <int BN>
-__global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid_constant__ GemmParams p) {
+// Dequantise one 16-byte unit of an A tile (row r, columns 8u .. 8u+7 of the
+// k-block) from a raw stage: 8 consecutive columns of one row sit in two
+// neighbouring lanes' words of the packed chunk (4 columns each) and share one
+// 32-block scale.  half: which 64 columns of a Q4 chunk (128 columns) this k-block is.
+template <int FMT>
+__device__ __forceinline__ uint4 dequant_unit(const uint32_t* __restrict__ qw, const float* __restrict__ sc, int r,
+                                              int u, int half) {
+  const int gl = r >> 3, n = r & 7;
+  const int q0 = (u & 1) * 2;
+  float q[8];
+  float d;
+  if (FMT == IL_Q8) {
+    const int base = gl * 128 + (4 * n + q0) * 4 + (u >> 1);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // lanes q0 and q0 + 1
+      uint32_t p01, p23;
+      q8_word_to_f16x2(qw[base + 4 * h], p01, p23);
+      q[4 * h] = f16_lo(p01);
+      q[4 * h + 1] = f16_hi(p01);
+      q[4 * h + 2] = f16_lo(p23);
+      q[4 * h + 3] = f16_hi(p23);
+    }
+    d = sc[gl * 16 + n * 2 + (u >> 2)];
+  } else {
+    const int w = 2 * half + (u >> 2), sub = (u >> 1) & 1;
+    const int base = gl * 128 + (4 * n + q0) * 4 + w;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t prs[4];
+      q4_word_to_f16x2(qw[base + 4 * h], prs);
+      const uint32_t p01 = sub ? prs[2] : prs[0], p23 = sub ? prs[3] : prs[1];  // no local-memory indexing
+      q[4 * h] = f16_lo(p01);
+      q[4 * h + 1] = f16_hi(p01);
+      q[4 * h + 2] = f16_lo(p23);
+      q[4 * h + 3] = f16_hi(p23);
+    }
+    d = sc[gl * 32 + n * 4 + w];
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(d, q[2 * i]), __fmul_rn(d, q[2 * i + 1]));
+    o[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int BN, int FMT>
+__global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr bool kQ = FMT != IL_BF16;
   constexpr uint32_t kABytes = kBM * kBK * 2;
   constexpr uint32_t kBBytes = BN * kBK * 2;
   constexpr uint32_t kStageBytes = kABytes + kBBytes;
   constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
+  // Q4: one raw stage (a 128-column chunk) feeds two k-blocks
+  constexpr int kKbPerRaw = FMT == IL_Q4 ? 2 : 1;
+  constexpr uint32_t kRawTx = kRawQuantBytes + 16u * scales_per_chunk(FMT) * 4u;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint8_t* raw = smem + kStages * kStageBytes;  // Q8/Q4 only
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + (kQ ? kRawStages * kRawStageBytes : 0));
   uint64_t* full = bars;                // [kStages]
   uint64_t* empty = bars + kStages;     // [kStages]
   uint64_t* tfull = bars + 2 * kStages; // [2]
   uint64_t* tempty = tfull + 2;         // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* raw_full = tempty + 2;      // [kRawStages]
+  uint64_t* raw_empty = raw_full + kRawStages;  // [kRawStages]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(raw_empty + kRawStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -215,12 +287,17 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
+      // Q8/Q4: the x tile's bytes plus one arrival per dequantising warp
+      mbar_init(smem_u32(&full[s]), kQ ? 1 + kXfWarps : 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
       mbar_init(smem_u32(&tempty[b]), 4);
+    }
+    for (int r = 0; r < kRawStages; ++r) {
+      mbar_init(smem_u32(&raw_full[r]), 1);
+      mbar_init(smem_u32(&raw_empty[r]), kXfWarps);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -242,25 +319,100 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) gemm_bf16_kernel(const __grid
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && !p.stall_producer) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.xmap)) : "memory");
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, rstage = 0;
+      uint32_t phase = 0, rphase = 0;
       const int units = p.total_tiles * p.splits;
-      for (int unit = blockIdx.x; unit < units && !*abort_flag; unit += gridDim.x) {
+      bool ok = true;
+      for (int unit = blockIdx.x; ok && unit < units && !*abort_flag; unit += gridDim.x) {
         int tile, split, kb0, kb1, job, mt, nt;
         unit_range(p, unit, tile, split, kb0, kb1);
         locate_tile(p, tile, job, mt, nt);
         const CUtensorMap* wm = &p.wmap[job];
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.status, kStProducer)) break;
+          if (kQ && kb % kKbPerRaw == 0) {
+            // packed quants + scales of row groups 16*mt .. +15, chunk kb / kKbPerRaw
+            if (!mbar_wait(smem_u32(&raw_empty[rstage]), rphase ^ 1, abort_flag, p.status, kStProducer)) {
+              ok = false;
+              break;
+            }
+            const uint32_t rb = smem_u32(&raw_full[rstage]);
+            mbar_expect_tx(rb, kRawTx);
+            const uint32_t r_dst = smem_u32(raw + rstage * kRawStageBytes);
+            const int c = kb / kKbPerRaw;
+            tma_load_2d(r_dst, wm, c * 128, mt * 16, rb);
+            tma_load_2d(r_dst + kRawQuantBytes, &p.smap[job], c * scales_per_chunk(FMT), mt * 16, rb);
+            if (++rstage == kRawStages) {
+              rstage = 0;
+              rphase ^= 1;
+            }
+          }
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.status, kStProducer)) {
+            ok = false;
+            break;
+          }
           const uint32_t fb = smem_u32(&full[stage]);
-          mbar_expect_tx(fb, kStageBytes);
           const uint32_t a_dst = smem_u32(tiles + stage * kStageBytes);
-          tma_load_2d(a_dst, wm, kb * kBK, mt * kBM, fb);
+          if (kQ) {
+            mbar_expect_tx(fb, kBBytes);
+          } else {
+            mbar_expect_tx(fb, kStageBytes);
+            tma_load_2d(a_dst, wm, kb * kBK, mt * kBM, fb);
+          }
           tma_load_2d(a_dst + kABytes, &p.xmap, kb * kBK, nt * BN, fb);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
+        }
+      }
+    }
+  } else if (kQ && warp >= 6) {
+    // ------------------------------------------------------------ dequantise raw -> A tiles
+    const int xt = threadIdx.x - 6 * 32;  // 0 .. 32 * kXfWarps - 1
+    int stage = 0, rstage = 0;
+    uint32_t phase = 0, rphase = 0;
+    const int units = p.total_tiles * p.splits;
+    bool ok = true;
+    for (int unit = blockIdx.x; ok && unit < units && !*abort_flag; unit += gridDim.x) {
+      int tile, split, kb0, kb1;
+      unit_range(p, unit, tile, split, kb0, kb1);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (kb % kKbPerRaw == 0 &&
+            !mbar_wait(smem_u32(&raw_full[rstage]), rphase, abort_flag, p.status, kStTransform)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, p.status, kStTransform)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* rs = raw + rstage * kRawStageBytes;
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(rs);
+        const float* sc = reinterpret_cast<const float*>(rs + kRawQuantBytes);
+        uint8_t* a_tile = tiles + stage * kStageBytes;
+        const int half = kb % kKbPerRaw;
+#pragma unroll
+        for (int it = 0; it < (kBM * 8) / (32 * kXfWarps); ++it) {
+          // a warp covers 4 rows x 8 units: 512 contiguous bytes of the tile
+          const int idx = it * (32 * kXfWarps) + xt;
+          const int r = idx >> 3, u = idx & 7;
+          const uint4 v = dequant_unit<FMT>(qw, sc, r, u, half);
+          *reinterpret_cast<uint4*>(a_tile + r * 128 + ((u ^ (r & 7)) << 4)) = v;
+        }
+        // make the generic-proxy stores visible to the tensor core, then report
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&full[stage]));
+          if (half == kKbPerRaw - 1) mbar_arrive(smem_u32(&raw_empty[rstage]));
+        }
+        if (half == kKbPerRaw - 1 && ++rstage == kRawStages) {
+          rstage = 0;
+          rphase ^= 1;
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
         }
       }
     }
@@ -518,8 +670,10 @@ struct Plan {
   int splits, kb_per_split, total_tiles;
 };
 
-// Split-K only when the tiles alone leave SMs idle: estimated time = tensor work
-// spread over whole waves of units + traffic of writing and summing partials.
+// Split-K only when the tiles alone leave SMs idle: estimated time = the larger
+// of the tensor work spread over whole waves of units and the weight stream
+// (which splitting does not shorten), plus the traffic of writing and summing
+// partials.
 Plan plan_launch(int64_t t, int64_t n_in_pad, const GemmJob* jobs, int nj, int num_sms, bool allow_split) {
   Plan pl{1, 0, 0};
   const int n_tiles_n = (int)((t + kBN - 1) / kBN);
@@ -532,15 +686,20 @@ Plan plan_launch(int64_t t, int64_t n_in_pad, const GemmJob* jobs, int nj, int n
   pl.kb_per_split = num_kb;
   if (!allow_split) return pl;
   const double flops = 2.0 * (double)t * (double)n_in_pad * (double)sum_n_out;
+  const int fmt = jobs[0].w->format;
+  const double wbytes = (double)sum_n_out * (double)n_in_pad * (fmt == IL_BF16 ? 2.0 : fmt == IL_Q8 ? 1.125 : 0.625);
+  // a Q4 chunk spans two k-blocks: slices start on a chunk
+  const int align = fmt == IL_Q4 ? 2 : 1;
   double best = 1e30;
   // at most two slices: the partial-tile traffic of more slices costs more than it saves
   for (int s = 1; s <= 2 && s <= num_kb / 4; ++s) {
-    const int kbps = (num_kb + s - 1) / s;
+    const int kbps = ((num_kb + s - 1) / s + align - 1) / align * align;
     const int se = (num_kb + kbps - 1) / kbps;
     const int64_t units = (int64_t)pl.total_tiles * se;
     const int64_t waves = (units + num_sms - 1) / num_sms;
     const double eff = (double)units / ((double)waves * num_sms);
-    const double est = flops / (1.5e15 * eff) + (se > 1 ? 2.0 * se * (double)t * sum_n_out * 4.0 / 5.0e12 : 0.0);
+    const double est = std::max(flops / (1.5e15 * eff), wbytes / 6.0e12) +
+                       (se > 1 ? 2.0 * se * (double)t * sum_n_out * 4.0 / 5.0e12 : 0.0);
     if (est < best * 0.97 || s == 1) {
       if (s == 1 || est < best * 0.97) {
         best = est;
@@ -569,16 +728,48 @@ size_t gemm_workspace_bytes(int64_t t, int64_t n_in_pad, const GemmJob* jobs, in
   return need;
 }
 
-cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs,
-                             int n_jobs, cudaStream_t stream, int num_sms, unsigned* status, int* launches,
-                             void* ws, size_t ws_bytes) {
+namespace {
+
+// Packed Q8/Q4 quants as a 2D tensor of 32-bit words: one row per row group
+// (all its chunks back to back, 512 bytes each); box = one chunk x 16 groups.
+bool make_quant_map(CUtensorMap* m, const PackedWeight& w) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)w.n_chunks * 128, (cuuint64_t)w.n_groups};
+  const cuuint64_t strides[1] = {(cuuint64_t)w.n_chunks * 512};
+  const cuuint32_t box[2] = {128, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, w.quants, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Packed scales: one row per row group, scales_per_chunk floats per chunk.
+bool make_scale_map(CUtensorMap* m, const PackedWeight& w) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const int spc = scales_per_chunk(w.format);
+  const cuuint64_t dims[2] = {(cuuint64_t)w.n_chunks * spc, (cuuint64_t)w.n_groups};
+  const cuuint64_t strides[1] = {(cuuint64_t)w.n_chunks * spc * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)spc, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, w.scales, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT>
+cudaError_t launch_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs, int n_jobs,
+                            cudaStream_t stream, int num_sms, unsigned* status, int* launches, void* ws,
+                            size_t ws_bytes) {
   constexpr int BN = kBN;
-  constexpr size_t smem = (size_t)kStages * (kBM * kBK * 2 + BN * kBK * 2) + 1024 + 256;
+  constexpr size_t smem = (size_t)kStages * (kBM * kBK * 2 + BN * kBK * 2) +
+                          (FMT == IL_BF16 ? 0 : (size_t)kRawStages * kRawStageBytes) + 1024 + 256;
   static unsigned long long attr_set = 0;  // one bit per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !(attr_set & (1ull << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     attr_set |= 1ull << dev;
@@ -617,9 +808,12 @@ cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
     int tiles = 0;
     for (int j = 0; j < nj; ++j) {
       const PackedWeight& w = *jobs[j0 + j].w;
-      if (!make_map(&p.wmap[j], w.quants, (uint64_t)w.n_in_pad, (uint64_t)w.n_out_pad, (uint64_t)w.n_in_pad, kBK,
-                    kBM))
-        return cudaErrorInvalidValue;
+      if (w.format != FMT || w.n_in_pad != n_in_pad) return cudaErrorInvalidValue;
+      const bool mapped = FMT == IL_BF16
+                              ? make_map(&p.wmap[j], w.quants, (uint64_t)w.n_in_pad, (uint64_t)w.n_out_pad,
+                                         (uint64_t)w.n_in_pad, kBK, kBM)
+                              : make_quant_map(&p.wmap[j], w) && make_scale_map(&p.smap[j], w);
+      if (!mapped) return cudaErrorInvalidValue;
       p.y[j] = jobs[j0 + j].y;
       p.n_out[j] = (int)w.n_out;
       if (w.glu) p.glu_mask |= 1u << j;
@@ -635,16 +829,30 @@ cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreadsGemm);
+    cfg.blockDim = dim3(gemm_threads(FMT));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = kUsePdl ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_bf16_kernel<BN>, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, FMT>, p);
     if (launches) ++*launches;
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int fmt, const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs,
+                        int n_jobs, cudaStream_t stream, int num_sms, unsigned* status, int* launches, void* ws,
+                        size_t ws_bytes) {
+  if (fmt == IL_BF16)
+    return launch_gemm_fmt<IL_BF16>(xb, t, n_in_pad, jobs, n_jobs, stream, num_sms, status, launches, ws, ws_bytes);
+  if (fmt == IL_Q8)
+    return launch_gemm_fmt<IL_Q8>(xb, t, n_in_pad, jobs, n_jobs, stream, num_sms, status, launches, ws, ws_bytes);
+  if (fmt == IL_Q4)
+    return launch_gemm_fmt<IL_Q4>(xb, t, n_in_pad, jobs, n_jobs, stream, num_sms, status, launches, ws, ws_bytes);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace il

@@ -57,21 +57,14 @@ std::mutex g_dev_mu;
 std::map<int, DeviceState> g_devices;
 
 // Scratch of the tensor-core path, one set per (device, stream): the bf16 copy
-// of x, the split-K workspace, and bf16 copies of Q8/Q4 weights at prefill sizes.
+// of x and the split-K workspace.
 struct Scratch {
   void* ptr = nullptr;
   size_t bytes = 0;
   void* ws = nullptr;
   size_t ws_bytes = 0;
-  void* wq = nullptr;
-  size_t wq_bytes = 0;
 };
 
-// Token counts above which a batch takes the tensor-core path: bf16 weights as
-// they are; Q8/Q4 weights after a dequantisation to bf16 (worth its extra pass
-// over the weight only once the decode kernel would stream it three times).
-constexpr int64_t kGemmMinT = 9;
-constexpr int64_t kGemmMinTQuant = 17;
 std::mutex g_scratch_mu;
 std::map<std::pair<int, cudaStream_t>, Scratch> g_scratch;
 
@@ -168,29 +161,6 @@ int get_scratch(int dev, cudaStream_t stream, size_t bytes, void** out) {
     s.bytes = want;
   }
   *out = s.ptr;
-  return IL_OK;
-}
-
-int get_wq(int dev, cudaStream_t stream, size_t bytes, void** out) {
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  Scratch& s = g_scratch[{dev, stream}];
-  if (s.wq_bytes < bytes) {
-    if (s.wq != nullptr) {
-      cudaError_t e = cudaStreamSynchronize(stream);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-      cudaFree(s.wq);
-      s.wq = nullptr;
-      s.wq_bytes = 0;
-    }
-    cudaError_t e = il_malloc(&s.wq, bytes);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      s.wq = nullptr;
-      return fail(IL_ERR_OOM, "allocating %zu bytes for bf16 copies of quantised weights failed", bytes);
-    }
-    s.wq_bytes = bytes;
-  }
-  *out = s.wq;
   return IL_OK;
 }
 
@@ -518,63 +488,41 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
     if (overlaps(sorted[i - 1].first, sorted[i - 1].second, sorted[i].first, sorted[i].second))
       return fail(IL_ERR_ARG, "il_matmul_batch: x and the y buffers must not overlap");
 
-  // ---- dispatch: large t -> cast x once + tensor-core GEMM (Q8/Q4 weights first
-  // dequantised to bf16 scratch); everything else -> decode kernel (token groups
-  // of 8), one launch per format present.
+  // ---- dispatch: large t -> cast x once + one tensor-core GEMM launch per format
+  // (Q8/Q4 weights are dequantised in shared memory inside it); everything else
+  // -> decode kernel (token groups of 8), one launch per format present.
   int launches = 0;
   cudaError_t e = cudaSuccess;
   const bool gemm_bf16 = t >= kGemmMinT;
   const bool gemm_quant = t >= kGemmMinTQuant;
-  std::vector<PackedWeight> deq;  // bf16 views of Q8/Q4 weights (host descriptors)
   if (gemm_bf16) {
-    std::vector<GemmJob> gj;
-    std::vector<int> qidx;
+    std::vector<GemmJob> gj[3];
     int64_t n_in_pad = 0;
-    size_t wq_bytes = 0;
     for (int j = 0; j < n_jobs; ++j) {
       const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[j].w);
       n_in_pad = w->n_in_pad;
-      if (w->format == IL_BF16) {
-        gj.push_back(GemmJob{w, jobs[j].y});
-      } else if (gemm_quant) {
-        qidx.push_back(j);
-        wq_bytes += (size_t)w->n_out_pad * (size_t)w->n_in_pad * 2;
-      }
+      if (w->format == IL_BF16 || gemm_quant) gj[w->format].push_back(GemmJob{w, jobs[j].y});
     }
-    if (!qidx.empty()) {
-      void* wq = nullptr;
-      const int rcq = get_wq(dev, stream, wq_bytes, &wq);
-      if (rcq != IL_OK) return rcq;
-      deq.reserve(qidx.size());
-      size_t off = 0;
-      for (int j : qidx) {
-        const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[j].w);
-        PackedWeight v = *w;
-        v.format = IL_BF16;
-        v.quants = static_cast<uint8_t*>(wq) + off;
-        v.scales = nullptr;
-        off += (size_t)w->n_out_pad * (size_t)w->n_in_pad * 2;
-        if (e == cudaSuccess) e = launch_dequant_bf16(*w, reinterpret_cast<__nv_bfloat16*>(v.quants), stream);
-        if (e == cudaSuccess) ++launches;
-        deq.push_back(v);
-      }
-      for (size_t i = 0; i < qidx.size(); ++i) gj.push_back(GemmJob{&deq[i], jobs[qidx[i]].y});
-    }
-    if (e == cudaSuccess && !gj.empty()) {
+    if (!gj[0].empty() || !gj[1].empty() || !gj[2].empty()) {
       void* xb = nullptr;
       const int rc = get_scratch(dev, stream, (size_t)t * (size_t)n_in_pad * 2, &xb);
       if (rc != IL_OK) return rc;
       void* ws = nullptr;
-      size_t ws_bytes = gemm_workspace_bytes(t, n_in_pad, gj.data(), (int)gj.size(), ds->num_sms);
+      size_t ws_bytes = 0;
+      for (int f = 0; f < 3; ++f)
+        if (!gj[f].empty())
+          ws_bytes = std::max(ws_bytes, gemm_workspace_bytes(t, n_in_pad, gj[f].data(), (int)gj[f].size(),
+                                                             ds->num_sms));
       if (ws_bytes > 0) {
         const int rc2 = get_workspace(dev, stream, ws_bytes, &ws, &ws_bytes);
         if (rc2 != IL_OK) return rc2;
       }
       e = launch_cast_bf16(x, t, n_in, n_in_pad, static_cast<__nv_bfloat16*>(xb), stream);
       if (e == cudaSuccess) ++launches;
-      if (e == cudaSuccess)
-        e = launch_gemm_bf16(static_cast<const __nv_bfloat16*>(xb), t, n_in_pad, gj.data(), (int)gj.size(), stream,
-                             ds->num_sms, ds->status, &launches, ws, ws_bytes);
+      for (int f = 0; f < 3 && e == cudaSuccess; ++f)
+        if (!gj[f].empty())
+          e = launch_gemm(f, static_cast<const __nv_bfloat16*>(xb), t, n_in_pad, gj[f].data(), (int)gj[f].size(),
+                          stream, ds->num_sms, ds->status, &launches, ws, ws_bytes);
     }
   }
   for (int fmt = IL_BF16; fmt <= IL_Q4 && e == cudaSuccess; ++fmt) {

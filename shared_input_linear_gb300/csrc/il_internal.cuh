@@ -169,26 +169,29 @@ __device__ __forceinline__ float gelu_mul(float g, float u) {
 // ---------------------------------------------------------------------------
 cudaError_t launch_pack(const PackedWeight& w, const uint8_t* staging, cudaStream_t stream);
 cudaError_t launch_dequant(const PackedWeight& w, float* out, cudaStream_t stream);
-// Q8/Q4 weight -> bf16 [n_out_pad][n_in_pad] row-major (RNE of fp32(d*q)), for the
-// tensor-core path at prefill sizes.
-cudaError_t launch_dequant_bf16(const PackedWeight& w, __nv_bfloat16* out, cudaStream_t stream);
 cudaError_t launch_decode(int fmt, const DecodeParams& p, cudaStream_t stream, int num_sms,
                           int* launches);
 cudaError_t launch_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_in_pad,
                              __nv_bfloat16* out, cudaStream_t stream);
 
+// Token counts from which a batch takes the tensor-core path instead of the
+// decode kernel (which streams the weights once per 8 tokens).
+constexpr int64_t kGemmMinT = 9;        // bf16 weights
+constexpr int64_t kGemmMinTQuant = 17;  // Q8 / Q4 weights
+
 struct GemmJob {
   const PackedWeight* w;
   float* y;  // [t][w->n_out], or h [t][w->n_out / 2] when w->glu
 };
-// Tensor-core path for large t (bf16 weights): xb is x cast to bf16,
-// [t][n_in_pad], zero in the padding columns.
+// Tensor-core path for large t: xb is x cast to bf16, [t][n_in_pad], zero in the
+// padding columns.  Every job has format `fmt` (bf16 weights are tiled as they
+// are; Q8/Q4 weights are dequantised to bf16 in shared memory inside the kernel).
 // ws / ws_bytes: split-K workspace (counters, then fp32 partial tiles); with
 // nullptr the kernel never splits K.  gemm_workspace_bytes gives the size the
 // launch plan wants (0 when no launch splits K).
-cudaError_t launch_gemm_bf16(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad,
-                             const GemmJob* jobs, int n_jobs, cudaStream_t stream, int num_sms,
-                             unsigned* status, int* launches, void* ws, size_t ws_bytes);
+cudaError_t launch_gemm(int fmt, const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs,
+                        int n_jobs, cudaStream_t stream, int num_sms, unsigned* status, int* launches, void* ws,
+                        size_t ws_bytes);
 size_t gemm_workspace_bytes(int64_t t, int64_t n_in_pad, const GemmJob* jobs, int n_jobs, int num_sms);
 
 }  // namespace il

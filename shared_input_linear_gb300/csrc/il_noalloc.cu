@@ -115,8 +115,8 @@ extern "C" int il_matmul_batch_noalloc(const float* x, int64_t t, int64_t n_in, 
     e = launch_cast_bf16(x, t, n_in, n_in_pad, xb, stream);
     if (e == cudaSuccess) ++launches;
     if (e == cudaSuccess)
-      e = launch_gemm_bf16(xb, t, n_in_pad, gj.data(), (int)gj.size(), stream, slot->num_sms, slot->status,
-                           &launches, nullptr, 0);
+      e = launch_gemm(IL_BF16, xb, t, n_in_pad, gj.data(), (int)gj.size(), stream, slot->num_sms, slot->status,
+                      &launches, nullptr, 0);
   }
   // decode path (t <= 8, or Q8/Q4 weights): needs no scratch
   for (int fmt = IL_BF16; fmt <= IL_Q4 && e == cudaSuccess; ++fmt) {

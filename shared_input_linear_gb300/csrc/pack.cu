@@ -156,69 +156,6 @@ __global__ void dequant_kernel(int fmt, const uint8_t* __restrict__ wq, const fl
   }
 }
 
-// Q8/Q4 weight -> bf16 row-major [n_out_pad][n_in_pad] (round to nearest even of
-// fp32(d*q)), the layout the tensor-core kernel tiles.  One thread writes 8
-// consecutive columns of one row: they sit in two neighbouring lanes' words of
-// one chunk (4 columns each) and share one 32-block scale.
-__global__ void dequant_bf16_kernel(int fmt, const uint8_t* __restrict__ wq, const float* __restrict__ ws,
-                                    int64_t n_out_pad, int64_t n_in_pad, int64_t n_chunks,
-                                    __nv_bfloat16* __restrict__ out) {
-  const int64_t per_row = n_in_pad / 8;
-  const int64_t total = n_out_pad * per_row;
-  grid_dep_wait();  // the scratch may still be read by the previous kernel
-  const uint32_t* words = reinterpret_cast<const uint32_t*>(wq);
-  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < total;
-       v += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = v / per_row;
-    const int64_t k = (v - r * per_row) * 8;
-    const int64_t g = r >> 3;
-    const int n = (int)(r & 7);
-    float q[8];
-    float d;
-    if (fmt == IL_Q8) {
-      const int64_t c = k >> 6;
-      const int kk = (int)(k & 63);
-      const int i = kk >> 4, q0 = (kk & 15) >> 2;  // q0 is 0 or 2
-      const int64_t base = ((g * n_chunks + c) * 32 + 4 * n + q0) * 4 + i;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {  // lanes q0 and q0 + 1
-        uint32_t p01, p23;
-        q8_word_to_f16x2(words[base + 4 * h], p01, p23);
-        q[4 * h] = f16_lo(p01);
-        q[4 * h + 1] = f16_hi(p01);
-        q[4 * h + 2] = f16_lo(p23);
-        q[4 * h + 3] = f16_hi(p23);
-      }
-      d = ws[((g * n_chunks + c) * 4 + (n >> 1)) * 4 + (n & 1) * 2 + (kk >> 5)];
-    } else {
-      const int64_t c = k >> 7;
-      const int kk = (int)(k & 127);
-      const int w = kk >> 5, sub = (kk & 31) >> 4, q0 = (kk & 15) >> 2;
-      const int64_t base = ((g * n_chunks + c) * 32 + 4 * n + q0) * 4 + w;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t prs[4];
-        q4_word_to_f16x2(words[base + 4 * h], prs);
-        const uint32_t p01 = prs[2 * sub];      // columns j = 0, 1
-        const uint32_t p23 = prs[2 * sub + 1];  // columns j = 2, 3
-        q[4 * h] = f16_lo(p01);
-        q[4 * h + 1] = f16_hi(p01);
-        q[4 * h + 2] = f16_lo(p23);
-        q[4 * h + 3] = f16_hi(p23);
-      }
-      d = ws[((g * n_chunks + c) * 4 + (n >> 1)) * 8 + (n & 1) * 4 + w];
-    }
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(d, q[2 * i]), __fmul_rn(d, q[2 * i + 1]));
-      o[i] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    *reinterpret_cast<uint4*>(out + r * n_in_pad + k) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-  grid_dep_launch();
-}
-
 int grid_for(int64_t work) {
   int64_t g = (work + 255) / 256;
   if (g > 65536) g = 65536;
@@ -244,20 +181,6 @@ cudaError_t launch_pack(const PackedWeight& w, const uint8_t* staging, cudaStrea
                                                          w.n_in, w.n_groups, w.n_chunks);
   }
   return cudaGetLastError();
-}
-
-cudaError_t launch_dequant_bf16(const PackedWeight& w, __nv_bfloat16* out, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(grid_for(w.n_out_pad * (w.n_in_pad / 8)));
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = kUsePdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, dequant_bf16_kernel, w.format, (const uint8_t*)w.quants, (const float*)w.scales,
-                            w.n_out_pad, w.n_in_pad, w.n_chunks, out);
 }
 
 cudaError_t launch_dequant(const PackedWeight& w, float* out, cudaStream_t stream) {

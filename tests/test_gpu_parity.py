@@ -86,6 +86,19 @@ def test_many_tokens(sil, fmt, t):
     assert_parity(b, ys, "many tokens")
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+@pytest.mark.parametrize("t,n_in,n_outs", [(17, 96, (1000, 136, 8)), (100, 1056, (300, 7)),
+                                           (300, 4128, (264,)), (64, 8192, (200,)),
+                                           (40, 12288, (128, 72))])
+def test_tensor_core_shapes(sil, fmt, t, n_in, n_outs):
+    # the tensor-core kernel (t >= 17 for every format; Q8/Q4 dequantised in shared
+    # memory): padded K, ragged row tiles, several jobs, split K at the few-tile shapes
+    b = wl.make_batch(n_in, n_outs, t, fmt, seed=n_in + t)
+    ys, guards = run(sil, b)
+    assert guards
+    assert_parity(b, ys, "tensor-core shapes")
+
+
 def test_bf16_odd_k(sil):
     # bf16 allows any n_in that is a multiple of 8
     for n_in in (8, 40, 264):
