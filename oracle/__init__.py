@@ -78,6 +78,12 @@ class Oracle:
         lib.oracle_gelu.restype = ctypes.c_double
         lib.oracle_gelu_mul.argtypes = [vp, vp, i64, vp]
         lib.oracle_gelu_mul.restype = None
+        lib.oracle_centroid_select.argtypes = [vp, i64, i64, vp, i64, vp, vp]
+        lib.oracle_centroid_select.restype = ctypes.c_int
+        lib.oracle_cluster_scores.argtypes = [vp, i64, i64, vp, i64, vp, i64, vp, vp, vp]
+        lib.oracle_cluster_scores.restype = ctypes.c_int
+        lib.oracle_first_max.argtypes = [vp, i64]
+        lib.oracle_first_max.restype = i64
         self.lib = lib
 
     def weight_bytes(self, fmt, n_out: int, n_in: int) -> int:
@@ -161,6 +167,54 @@ class Oracle:
         return self.gelu_mul(g, u), g, u, mag_g, mag_u
 
 
+    # -- centroid-masked LM head (oxinfer 0.0.1, src/drafter.rs, end of Drafter::step)
+    def centroid_select(self, centroids: np.ndarray, n_cent: int, h: int, x: np.ndarray, k: int):
+        """Centroid logits (f64 ``[n_cent]``) and the ``k`` selected centroids in rank order."""
+        c = self._check_w(BF16, centroids, n_cent, h)
+        x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+        if x.size != h:
+            raise ValueError("x must hold h values")
+        cl = np.empty(n_cent, dtype=np.float64)
+        sel = np.empty(k, dtype=np.int64)
+        if self.lib.oracle_centroid_select(_ptr(c), n_cent, h, _ptr(x), k, _ptr(cl), _ptr(sel)) != 0:
+            raise ValueError("oracle_centroid_select rejected its arguments")
+        return cl, sel
+
+    def cluster_scores(self, embed: np.ndarray, vocab: int, h: int, ordering: np.ndarray, per: int,
+                       sel: np.ndarray, x: np.ndarray):
+        """Exact logits (and ``mag``) of the tokens of the clusters ``sel``, (rank, position) order."""
+        e = self._check_w(BF16, embed, vocab, h)
+        ordering = np.ascontiguousarray(ordering, dtype=np.uint32)
+        sel = np.ascontiguousarray(sel, dtype=np.int64)
+        x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+        k = sel.size
+        scores = np.empty(k * per, dtype=np.float64)
+        mag = np.empty(k * per, dtype=np.float64)
+        rc = self.lib.oracle_cluster_scores(_ptr(e), vocab, h, _ptr(ordering), per, _ptr(sel), k, _ptr(x),
+                                            _ptr(scores), _ptr(mag))
+        if rc != 0:
+            raise ValueError("oracle_cluster_scores: an ordering entry is out of range")
+        return scores, mag
+
+    def first_max(self, scores: np.ndarray) -> int:
+        """Position of the first strict maximum above -inf, or -1."""
+        s = np.ascontiguousarray(scores, dtype=np.float64)
+        return int(self.lib.oracle_first_max(_ptr(s), s.size))
+
+    def centroid_head(self, centroids, n_cent, embed, vocab, h, ordering, x, top_k):
+        """The whole head: returns a dict with cl, sel, scores, mag, position, token, score."""
+        k = min(int(top_k), int(n_cent))
+        per = vocab // n_cent
+        cl, sel = self.centroid_select(centroids, n_cent, h, x, k)
+        scores, mag = self.cluster_scores(embed, vocab, h, ordering, per, sel, x)
+        pos = self.first_max(scores)
+        ordering = np.asarray(ordering, dtype=np.uint32)
+        token = 0 if pos < 0 else int(ordering[sel[pos // per] * per + pos % per])
+        score = -np.inf if pos < 0 else float(scores[pos])
+        return {"cl": cl, "sel": sel, "scores": scores, "mag": mag, "position": pos, "token": token,
+                "score": score, "per": per}
+
+
 def _fmt(fmt) -> int:
     return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
 
@@ -201,6 +255,10 @@ def matmul_batch(x: np.ndarray, jobs):
     """
     n_in = x.shape[1]
     return [linear(fmt, w, n_out, n_in, x) for fmt, w, n_out in jobs]
+
+
+def centroid_head(centroids, n_cent, embed, vocab, h, ordering, x, top_k):
+    return default().centroid_head(centroids, n_cent, embed, vocab, h, ordering, x, top_k)
 
 
 def gelu_mul(g, u) -> np.ndarray:

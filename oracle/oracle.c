@@ -160,3 +160,86 @@ double oracle_gelu(double g) {
 void oracle_gelu_mul(const double* g, const double* u, int64_t n, double* h) {
   for (int64_t i = 0; i < n; ++i) h[i] = oracle_gelu(g[i]) * u[i];
 }
+
+/* ---------------------------------------------------------------------------
+ * Centroid-masked LM head (oxinfer 0.0.1, src/drafter.rs, end of
+ * `Drafter::step`): logits of the centroids, the top-k centroids, exact logits
+ * over the tokens of their clusters, and the first maximum.
+ *   centroids : bf16 [n_cent][h]; embed: bf16 [vocab][h]; ordering: u32 [vocab],
+ *   cluster c owning ordering[c*per .. (c+1)*per), per = vocab / n_cent.
+ * Readings where the page leaves the step open (the selection there is
+ * `select_nth_unstable_by`, whose order and tie handling are unspecified):
+ *   - the k selected centroids are the k largest logits, ties to the lower
+ *     centroid index, NaN below every number; they are taken in that rank
+ *     order, which is also the order the final scan visits them;
+ *   - the final scan starts from (-inf, token 0) and takes a score only when it
+ *     is strictly greater, so the first maximum in (rank, position) order wins,
+ *     NaN and -inf never win, and with no winner the token is 0.
+ * ------------------------------------------------------------------------- */
+
+/* Rank of centroid a before centroid b: larger logit first, NaN last, ties to
+ * the lower index. */
+static int ranks_before(const double* cl, int64_t a, int64_t b) {
+  const int na = isnan(cl[a]), nb = isnan(cl[b]);
+  if (na != nb) return nb;            /* the number ranks before the NaN */
+  if (!na && cl[a] != cl[b]) return cl[a] > cl[b];
+  return a < b;
+}
+
+/* Step 1 and 2: centroid logits (f64) and the k selected centroids in rank order
+ * (selection by repeated scans: plain and slow on purpose). */
+int oracle_centroid_select(const void* centroids, int64_t n_cent, int64_t h, const float* x, int64_t k,
+                           double* cl, int64_t* sel) {
+  if (n_cent < 1 || h < 1 || k < 1 || k > n_cent) return -1;
+  for (int64_t c = 0; c < n_cent; ++c) {
+    double acc = 0.0;
+    for (int64_t i = 0; i < h; ++i)
+      acc += (double)x[i] * (double)weight_at(ORACLE_BF16, (const uint8_t*)centroids, n_cent, h, c, i);
+    cl[c] = acc;
+  }
+  for (int64_t r = 0; r < k; ++r) {
+    int64_t best = -1;
+    for (int64_t c = 0; c < n_cent; ++c) {
+      int taken = 0;
+      for (int64_t q = 0; q < r; ++q) taken |= sel[q] == c;
+      if (taken) continue;
+      if (best < 0 || ranks_before(cl, c, best)) best = c;
+    }
+    sel[r] = best;
+  }
+  return 0;
+}
+
+/* Step 3: the exact logit of every token of the selected clusters, in
+ * (rank, position) order: scores[i*per + j] = embed[ordering[sel[i]*per + j]] . x,
+ * with mag = sum |embed . x| for the tolerance. */
+int oracle_cluster_scores(const void* embed, int64_t vocab, int64_t h, const uint32_t* ordering, int64_t per,
+                          const int64_t* sel, int64_t k, const float* x, double* scores, double* mag) {
+  for (int64_t i = 0; i < k; ++i)
+    for (int64_t j = 0; j < per; ++j) {
+      const uint32_t tok = ordering[sel[i] * per + j];
+      if ((int64_t)tok >= vocab) return -1;
+      double acc = 0.0, m = 0.0;
+      for (int64_t e = 0; e < h; ++e) {
+        const double p = (double)x[e] * (double)weight_at(ORACLE_BF16, (const uint8_t*)embed, vocab, h, tok, e);
+        acc += p;
+        m += fabs(p);
+      }
+      scores[i * per + j] = acc;
+      mag[i * per + j] = m;
+    }
+  return 0;
+}
+
+/* Step 4: the first maximum, strict '>' from (-inf, token 0).  Returns the
+ * winning position i*per + j, or -1 when nothing beats -inf. */
+int64_t oracle_first_max(const double* scores, int64_t n) {
+  double best = -INFINITY;
+  int64_t at = -1;
+  for (int64_t p = 0; p < n; ++p)
+    if (scores[p] > best) {
+      best = scores[p];
+      at = p;
+    }
+  return at;
+}

@@ -289,11 +289,91 @@ def pin_gate_up_one_hot(orc):
             assert np.all(np.abs(h[0] - ref) <= 5e-4 * np.abs(du[:, k]) + 1e-15), (fmt, k)
 
 
+# ---------------------------------------------------------------------------
+# centroid-masked LM head (oxinfer 0.0.1, src/drafter.rs, end of Drafter::step)
+# ---------------------------------------------------------------------------
+def _rows_bf16(rows, h=8):
+    w = np.zeros((len(rows), h), dtype=np.float32)
+    for r, vals in enumerate(rows):
+        w[r, :len(vals)] = vals
+    return wl.encode_bf16(wl.bf16_bits(torch.from_numpy(w)))
+
+
+def _head_example():
+    # hand-built: x = (1, 2, 0, ...), so a row (a, b, ...) scores a + 2b
+    x = np.zeros(8, dtype=np.float32)
+    x[:2] = (1.0, 2.0)
+    centroids = _rows_bf16([(1, 0), (0, 1), (3, 0), (1, 0)])       # logits 1, 2, 3, 1
+    ordering = np.array([5, 1, 7, 0, 3, 6, 2, 4], dtype=np.uint32)   # c0 {5,1} c1 {7,0} c2 {3,6} c3 {2,4}
+    embed = _rows_bf16([(0, 0), (-1, 0), (10, 0), (1, 1), (10, 0), (4, 0), (2, 0.5), (0, 1.5)])
+    return x, centroids, embed, ordering
+
+
+def pin_centroid_head_worked_example(orc):
+    # logits 1, 2, 3, 1: rank c2, c1, then the tie c0 / c3 goes to the lower index
+    x, cen, emb, order = _head_example()
+    r = orc.centroid_head(cen, 4, emb, 8, 8, order, x, 3)
+    assert list(r["cl"]) == [1.0, 2.0, 3.0, 1.0]
+    assert list(r["sel"]) == [2, 1, 0]
+    # clusters in rank order: c2 {3, 6}, c1 {7, 0}, c0 {5, 1}
+    assert list(r["scores"]) == [3.0, 3.0, 3.0, 0.0, 4.0, -1.0]
+    assert (r["position"], r["token"], r["score"]) == (4, 5, 4.0)
+    # k = 2: the three tied 3s, the first (token 3 at rank 0, position 0) wins
+    r = orc.centroid_head(cen, 4, emb, 8, 8, order, x, 2)
+    assert list(r["sel"]) == [2, 1] and (r["position"], r["token"]) == (0, 3)
+    # k = 4 reaches c3 {2, 4}, two tied 10s: the first, token 2
+    r = orc.centroid_head(cen, 4, emb, 8, 8, order, x, 4)
+    assert list(r["sel"]) == [2, 1, 0, 3] and (r["position"], r["token"], r["score"]) == (6, 2, 10.0)
+    # top_k above the centroid count is clamped
+    assert list(orc.centroid_head(cen, 4, emb, 8, 8, order, x, 9)["sel"]) == [2, 1, 0, 3]
+
+
+def pin_centroid_head_nan_and_empty(orc):
+    # a NaN centroid logit ranks below every number; NaN and -inf scores never win,
+    # and with no winner the token is 0 (the scan starts from (-inf, 0))
+    x, _, emb, order = _head_example()
+    cen = _rows_bf16([(1, 0), (float("nan"), 0), (3, 0), (-5, 0)])   # logits 1, NaN, 3, -5
+    r = orc.centroid_head(cen, 4, emb, 8, 8, order, x, 3)
+    assert list(r["sel"]) == [2, 0, 3]
+    assert orc.first_max(np.array([np.nan, -np.inf, np.nan])) == -1
+    assert orc.first_max(np.array([np.nan, 2.0, np.nan, 2.0, 1.0])) == 1
+    assert orc.first_max(np.array([-np.inf, -1e300])) == 1
+
+
+def pin_centroid_head_against_library(orc):
+    # random data with ties: the selection equals a lexicographic sort by (-logit,
+    # index) from numpy, the scores a float64 matmul of the gathered rows, and the
+    # winner numpy's argmax (which also returns the first maximum)
+    rng = np.random.default_rng(4)
+    n_cent, per, h = 16, 4, 24
+    vocab = n_cent * per
+    x = rng.integers(-3, 4, size=h).astype(np.float32)
+    cw = rng.integers(-2, 3, size=(n_cent, h)).astype(np.float32)
+    cw[5] = cw[3]                                   # a tie between two centroids
+    ew = rng.integers(-2, 3, size=(vocab, h)).astype(np.float32)
+    order = rng.permutation(vocab).astype(np.uint32)
+    cen = wl.encode_bf16(wl.bf16_bits(torch.from_numpy(cw)))
+    emb = wl.encode_bf16(wl.bf16_bits(torch.from_numpy(ew)))
+    for k in (1, 5, 16):
+        r = orc.centroid_head(cen, n_cent, emb, vocab, h, order, x, k)
+        cl = cw.astype(np.float64) @ x.astype(np.float64)
+        assert np.array_equal(r["cl"], cl)
+        want = np.lexsort((np.arange(n_cent), -cl))[:k]
+        assert list(r["sel"]) == list(want), k
+        rows = order[(want[:, None] * per + np.arange(per)[None, :]).reshape(-1)]
+        sc = ew[rows].astype(np.float64) @ x.astype(np.float64)
+        assert np.array_equal(r["scores"], sc)
+        pos = int(np.argmax(sc))
+        assert r["position"] == pos and r["token"] == int(rows[pos])
+
+
 ALL_PINS = [pin_weight_bytes, pin_bf16_exhaustive, pin_q8_exhaustive, pin_q4_exhaustive,
             pin_block_scale_index, pin_brute_force_small, pin_golden_files, pin_identity,
             pin_one_hot, pin_integer_exact, pin_library_crosscheck,
             pin_sampled_matches_definition, pin_gelu_against_erf, pin_gelu_identities,
-            pin_gelu_lipschitz, pin_gelu_mul_roles, pin_gate_up_one_hot]
+            pin_gelu_lipschitz, pin_gelu_mul_roles, pin_gate_up_one_hot,
+            pin_centroid_head_worked_example, pin_centroid_head_nan_and_empty,
+            pin_centroid_head_against_library]
 
 
 def _read_golden(path):
@@ -416,6 +496,10 @@ MUTANTS = {
     "gelu_wrong_constant": ("sqrt(2.0 / pi)", "sqrt(pi / 2.0)"),
     "gelu_sign": ("0.5 * g * (1.0 + tanh(inner))", "0.5 * g * (1.0 - tanh(inner))"),
     "gelu_mul_roles_swapped": ("h[i] = oracle_gelu(g[i]) * u[i];", "h[i] = oracle_gelu(u[i]) * g[i];"),
+    "centroid_tie_to_higher_index": ("  return a < b;\n}", "  return a > b;\n}"),
+    "centroid_nan_first": ("if (na != nb) return nb;", "if (na != nb) return na;"),
+    "first_max_takes_last": ("if (scores[p] > best) {", "if (scores[p] >= best) {"),
+    "cluster_offset_wrong": ("ordering[sel[i] * per + j]", "ordering[sel[i] + j]"),
 }
 
 
