@@ -355,6 +355,51 @@ def run_per_config(sil, torch, pk, only=None):
     return out
 
 
+def run_centroid_head(sil, torch, pk):
+    """The centroid-masked LM head on the dense vocab projection's shape: time per call,
+    with 8 copies of the centroids and 2 of the embedding rotating (more than L2)."""
+    c = wl.CENTROID_HEAD
+    inp = wl.make_head_inputs(c.h, c.vocab, c.n_cent, seed=0)
+    cws = [sil.upload_weight("bf16", inp.centroids, c.n_cent, c.h) for _ in range(8)]
+    ews = [sil.upload_weight("bf16", inp.embed, c.vocab, c.h) for _ in range(2)]
+    x = torch.from_numpy(inp.x).cuda()
+    od = torch.from_numpy(inp.ordering.view(np.int32)).cuda()
+    tok = torch.zeros(1, dtype=torch.int32, device="cuda")
+    score = torch.zeros(1, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            sil.centroid_head(x, cws[i % 8], ews[i % 2], od, c.top_k, tok, score, stream=stream)
+    torch.cuda.synchronize()
+    n = 64
+    launches0 = sil.get_stats()["launches"]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            sil.centroid_head(x, cws[i % 8], ews[i % 2], od, c.top_k, tok, score, stream=stream)
+    launches = (sil.get_stats()["launches"] - launches0) // n
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        for _ in range(3):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (3 * n)
+    k_rows = c.top_k * (c.vocab // c.n_cent)
+    moved = c.n_cent * c.h * 2 + k_rows * (c.h * 2 + 4)
+    del g
+    for w in cws + ews:
+        w.free()
+    return {"workload": c.name, "h": c.h, "vocab": c.vocab, "n_cent": c.n_cent, "top_k": c.top_k,
+            "us": round(us, 3), "launches_per_call": launches, "bytes_per_call": moved,
+            "gbs": round(moved / (us * 1e-6) / 1e9, 1),
+            "frac_hbm_measured": round(moved / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+            "dense_rows_bytes": c.vocab * c.h * 2}
+
+
 def run_dispatch(sil, torch):
     """Fixed cost of one submission (the pages quote ~0.15 ms per dispatch on Metal):
     host time of an eager il_matmul_batch call, the same call made synchronous, the
@@ -485,9 +530,11 @@ def main():
 
     per_config = None
     dispatch = None
+    lm_head = None
     if rank == 0 and world == 1 and not args.no_per_config:
         per_config = run_per_config(sil, torch, pk)
         dispatch = run_dispatch(sil, torch)
+        lm_head = run_centroid_head(sil, torch, pk)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -526,7 +573,7 @@ def main():
                 "roofline": roof, "e2e": {k: (round(v, 3) if isinstance(v, float) else v)
                                           for k, v in e2e.items()},
                 "gpu_launches": head["launches"], "clocks": clk, "cpu_baseline": cpu,
-                "per_config": per_config, "dispatch": dispatch}
+                "per_config": per_config, "dispatch": dispatch, "centroid_head": lm_head}
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

@@ -165,6 +165,40 @@ int il_matmul_batch_noalloc(const float* x, int64_t t, int64_t n_in, const il_jo
 il_weight* il_upload_gate_up(int format, const void* gate_ptr, const void* up_ptr, int64_t n_out,
                              int64_t n_in);
 
+/*
+ * il_centroid_head -- centroid-masked LM head (oxinfer 0.0.1, src/drafter.rs,
+ * end of `Drafter::step`): centroid logits cl = centroids * x, the top_k
+ * centroids, the exact logits of the tokens of their clusters, and the token
+ * of the first maximum.
+ *   x          : DEVICE fp32 [h] (one token), 16-byte aligned.
+ *   h          : width; must equal both handles' n_in (<= 32768).
+ *   centroids  : bf16 handle [n_cent][h], 1 <= n_cent <= 16384 (a plain weight).
+ *   embed      : bf16 handle [vocab][h], vocab a multiple of n_cent; cluster c
+ *                owns the tokens ordering[c*per .. (c+1)*per), per = vocab / n_cent.
+ *   ordering   : DEVICE u32 [vocab].  An entry >= vocab is skipped (never wins)
+ *                and flagged in the device status word (see below).
+ *   top_k      : >= 1; k = min(top_k, n_cent) clusters are scored.
+ *   token_out  : DEVICE u32 [1]: the winning token id.
+ *   score_out  : DEVICE fp32 [1] or NULL: its logit.
+ *   selected_out : DEVICE u32 [k] or NULL: the selected centroids in rank order.
+ *   scores_out : DEVICE fp32 [k*per] or NULL: every scored logit, index i*per + j
+ *                for the j-th token of the i-th selected cluster.
+ *   stream     : cudaStream_t (NULL = legacy default stream).
+ * Order and ties (the page selects with an unstable partition and scans with a
+ * strict '>'; this is the reading taken): centroids rank by larger logit, NaN
+ * last, ties to the lower index, and are scanned in that order; among equal
+ * logits the first in (rank, position) order wins; NaN and -inf never win, and
+ * with no winner the token is 0 and the score -inf.  Logits are fp32 sums of
+ * bf16 * fp32 products.  Asynchronous; three kernel launches (the centroid
+ * logits run as a one-job il_matmul_batch and are counted as a batch).  Calls
+ * on one stream are ordered; the library keeps per-stream scratch for it.
+ * An out-of-range ordering entry sets the status word, and il_check_device_status
+ * then returns IL_ERR_ARG.
+ */
+int il_centroid_head(const float* x, int64_t h, const il_weight* centroids, const il_weight* embed,
+                     const uint32_t* ordering, int64_t top_k, uint32_t* token_out, float* score_out,
+                     uint32_t* selected_out, float* scores_out, void* stream);
+
 /* 1 if the handle came from il_upload_gate_up, 0 if from il_upload_weight,
  * -1 for an invalid handle. */
 int il_weight_is_gate_up(const il_weight* w);
@@ -196,7 +230,9 @@ int il_dequantize_weight(const il_weight* w, float* dev_out, void* stream);
  * kernels set when they give up.  Synchronises `stream`.  Returns IL_OK, or
  * IL_ERR_DEVICE_TIMEOUT if a wait timed out since the last call; in that case
  * it also clears the library's split-K workspaces on the current device
- * (synchronously), so that later batches start from a clean state. */
+ * (synchronously), so that later batches start from a clean state.  Returns
+ * IL_ERR_ARG if no wait timed out but il_centroid_head met an ordering entry
+ * >= vocab. */
 int il_check_device_status(void* stream);
 
 /* Message of the last error on this thread ("" if none). */

@@ -79,6 +79,8 @@ def load() -> ctypes.CDLL:
         lib.il_matmul_batch_noalloc.restype = ci
         lib.il_upload_gate_up.argtypes = [ci, vp, vp, i64, i64]
         lib.il_upload_gate_up.restype = vp
+        lib.il_centroid_head.argtypes = [vp, i64, vp, vp, vp, i64, vp, vp, vp, vp, vp]
+        lib.il_centroid_head.restype = ci
         lib.il_weight_is_gate_up.argtypes = [vp]
         lib.il_weight_is_gate_up.restype = ci
         lib.il_free_weight.argtypes = [vp]
@@ -176,6 +178,20 @@ def upload_gate_up(fmt, gate, up, n_out: int, n_in: int) -> Weight:
 def is_gate_up(w) -> int:
     """``il_weight_is_gate_up``: 1, 0, or -1 for an invalid handle."""
     return int(load().il_weight_is_gate_up(w.handle if isinstance(w, Weight) else w))
+
+
+def centroid_head(x, centroids: Weight, embed: Weight, ordering, top_k: int, token_out, score_out=None,
+                  selected_out=None, scores_out=None, stream=None) -> None:
+    """``il_centroid_head`` on torch CUDA tensors: ``x`` fp32 ``[h]``, ``ordering`` int32/uint32
+    ``[vocab]``, ``token_out`` 32-bit ``[1]``; the optional outputs as documented in
+    ``include/il.h``.  Enqueued on ``stream`` (default: the current torch stream)."""
+    def ptr(t):
+        return 0 if t is None else t.data_ptr()
+    if not x.is_contiguous() or not ordering.is_contiguous():
+        raise ILError(-1, "x and ordering must be contiguous")
+    _check(load().il_centroid_head(ptr(x), int(x.numel()), centroids.handle, embed.handle, ptr(ordering),
+                                   int(top_k), ptr(token_out), ptr(score_out), ptr(selected_out),
+                                   ptr(scores_out), _stream_ptr(stream)))
 
 
 def free_weight(w: Weight) -> None:

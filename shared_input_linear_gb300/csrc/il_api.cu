@@ -191,6 +191,44 @@ int get_workspace(int dev, cudaStream_t stream, size_t bytes, void** out, size_t
   return IL_OK;
 }
 
+// Scratch of il_centroid_head, one set per (device, stream): centroid logits,
+// the selection, and the 64-bit best key + arrival counter (zero between calls).
+struct HeadScratch {
+  void* ptr = nullptr;
+  int64_t n_cent = 0, k = 0;
+};
+std::map<std::pair<int, cudaStream_t>, HeadScratch> g_head_scratch;
+
+constexpr size_t kHeadStateBytes = 256;  // best key (8 bytes) and counter, at the start
+
+int get_head_scratch(int dev, cudaStream_t stream, int64_t n_cent, int64_t k, uint8_t** out) {
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  HeadScratch& s = g_head_scratch[{dev, stream}];
+  if (s.n_cent < n_cent || s.k < k) {
+    if (s.ptr != nullptr) {
+      cudaError_t e = cudaStreamSynchronize(stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+      cudaFree(s.ptr);
+      s.ptr = nullptr;
+      s.n_cent = s.k = 0;
+    }
+    const int64_t nc = std::max(n_cent, (int64_t)1024), kk = std::max(k, (int64_t)256);
+    const size_t bytes = kHeadStateBytes + (size_t)nc * 4 + (size_t)kk * 4;
+    cudaError_t e = il_malloc(&s.ptr, bytes);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      s.ptr = nullptr;
+      return fail(IL_ERR_OOM, "allocating %zu bytes of LM-head scratch failed", bytes);
+    }
+    e = cudaMemsetAsync(s.ptr, 0, bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(LM-head scratch)");
+    s.n_cent = nc;
+    s.k = kk;
+  }
+  *out = static_cast<uint8_t*>(s.ptr);
+  return IL_OK;
+}
+
 bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
 
 }  // namespace
@@ -420,6 +458,7 @@ int il_check_device_status(void* stream) {
   if (e == cudaSuccess) e = cudaMemsetAsync(ds->status, 0, sizeof word, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "il_check_device_status");
+  if (word == kStatusBadToken) return fail(IL_ERR_ARG, "il_centroid_head met an ordering entry >= vocab");
   if (word != 0) {
     // a kernel that gave up may have left split-K arrival counters behind: clear
     // this device's workspaces so the next launches start from zero
@@ -565,6 +604,60 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
   g_stats.launches.fetch_add((uint64_t)launches);
   g_stats.weight_bytes.fetch_add(wbytes);
   g_stats.flops.fetch_add(flops);
+  return IL_OK;
+}
+
+int il_centroid_head(const float* x, int64_t h, const il_weight* centroids_h, const il_weight* embed_h,
+                     const uint32_t* ordering, int64_t top_k, uint32_t* token_out, float* score_out,
+                     uint32_t* selected_out, float* scores_out, void* stream_) {
+  clear_error();
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (x == nullptr || ordering == nullptr || token_out == nullptr)
+    return fail(IL_ERR_ARG, "il_centroid_head: x, ordering and token_out must not be NULL");
+  if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return fail(IL_ERR_ARG, "il_centroid_head: x is not 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(ordering) % 4 != 0 || reinterpret_cast<uintptr_t>(token_out) % 4 != 0 ||
+      reinterpret_cast<uintptr_t>(score_out) % 4 != 0 || reinterpret_cast<uintptr_t>(selected_out) % 4 != 0 ||
+      reinterpret_cast<uintptr_t>(scores_out) % 4 != 0)
+    return fail(IL_ERR_ARG, "il_centroid_head: outputs and ordering must be 4-byte aligned");
+  if (top_k < 1) return fail(IL_ERR_ARG, "il_centroid_head: top_k=%lld must be >= 1", (long long)top_k);
+  DeviceState* ds = nullptr;
+  const int dev = current_device(&ds);
+  if (dev < 0) return dev;
+  const PackedWeight* cw = reinterpret_cast<const PackedWeight*>(centroids_h);
+  const PackedWeight* ew = reinterpret_cast<const PackedWeight*>(embed_h);
+  if (cw == nullptr || ew == nullptr || !known_handle(centroids_h) || !known_handle(embed_h))
+    return fail(IL_ERR_HANDLE, "il_centroid_head: invalid weight handle");
+  if (cw->device != dev || ew->device != dev)
+    return fail(IL_ERR_HANDLE, "il_centroid_head: a weight lives on another device");
+  if (cw->format != IL_BF16 || ew->format != IL_BF16 || cw->glu || ew->glu)
+    return fail(IL_ERR_FORMAT, "il_centroid_head: centroids and embed must be plain bf16 weights");
+  if (h < 1 || h > kMaxHeadWidth || cw->n_in != h || ew->n_in != h)
+    return fail(IL_ERR_SHAPE, "il_centroid_head: h=%lld must equal both weights' n_in", (long long)h);
+  const int64_t n_cent = cw->n_out, vocab = ew->n_out;
+  if (n_cent > kMaxCentroids)
+    return fail(IL_ERR_UNSUPPORTED, "il_centroid_head: %lld centroids, at most %d", (long long)n_cent, kMaxCentroids);
+  if (vocab % n_cent != 0)
+    return fail(IL_ERR_SHAPE, "il_centroid_head: vocab=%lld is not a multiple of n_cent=%lld", (long long)vocab,
+                (long long)n_cent);
+  const int64_t k = std::min(top_k, n_cent);
+  const int64_t per = vocab / n_cent;
+  uint8_t* scratch = nullptr;
+  int rc = get_head_scratch(dev, stream, n_cent, k, &scratch);
+  if (rc != IL_OK) return rc;
+  float* cl = reinterpret_cast<float*>(scratch + kHeadStateBytes);
+  uint32_t* sel = selected_out != nullptr ? selected_out : reinterpret_cast<uint32_t*>(cl + std::max(n_cent, (int64_t)1024));
+  // 1. centroid logits: a one-job batch on the decode kernel
+  il_job job{centroids_h, n_cent, cl};
+  rc = il_matmul_batch(x, 1, h, &job, 1, stream_);
+  if (rc != IL_OK) return rc;
+  // 2-4. selection, cluster logits, first maximum
+  int launches = 0;
+  cudaError_t e = launch_lmhead(x, (int)h, cl, (int)n_cent, (int)k, *ew, ordering, (int)per, sel, scores_out,
+                                reinterpret_cast<unsigned long long*>(scratch),
+                                reinterpret_cast<unsigned*>(scratch + 8), token_out, score_out, ds->status, stream,
+                                ds->num_sms, &launches);
+  g_stats.launches.fetch_add((uint64_t)launches);
+  if (e != cudaSuccess) return cuda_fail(e, "il_centroid_head: launch");
   return IL_OK;
 }
 

@@ -194,4 +194,16 @@ cudaError_t launch_gemm(int fmt, const __nv_bfloat16* xb, int64_t t, int64_t n_i
                         size_t ws_bytes);
 size_t gemm_workspace_bytes(int64_t t, int64_t n_in_pad, const GemmJob* jobs, int n_jobs, int num_sms);
 
+// Centroid-masked LM head after the centroid logits cl [n_cent] are computed:
+// top-k selection (sel [k]), the gathered cluster logits (scores_out [k*per],
+// optional) and the first maximum (token_out, score_out optional).  best_key and
+// done are zero before the call and zero again after it.
+constexpr int kMaxCentroids = 16384;   // the selection sorts them in one CTA's shared memory
+constexpr unsigned kStatusBadToken = 0x100;  // status word: an ordering entry >= vocab was skipped
+constexpr int kMaxHeadWidth = 32768;   // x is staged in shared memory as fp32
+cudaError_t launch_lmhead(const float* x, int h, const float* cl, int n_cent, int k, const PackedWeight& embed,
+                          const uint32_t* ordering, int per, uint32_t* sel, float* scores_out,
+                          unsigned long long* best_key, unsigned* done, uint32_t* token_out, float* score_out,
+                          unsigned* status, cudaStream_t stream, int num_sms, int* launches);
+
 }  // namespace il

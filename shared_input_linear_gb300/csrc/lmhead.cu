@@ -1,0 +1,206 @@
+// lmhead.cu -- centroid-masked LM head (oxinfer 0.0.1, src/drafter.rs, end of
+// `Drafter::step`): the logits of the vocabulary's centroids pick the top-k
+// clusters, and only the tokens of those clusters get an exact logit; the
+// result is the first maximum.
+//
+//   1. cl = centroids . x               decode kernel (a one-job batch, t = 1)
+//   2. sel = top-k of cl                 topk_kernel: one CTA, bitonic sort of
+//                                        rank keys in shared memory
+//   3. score[i*per + j] =                cluster_score_kernel: one warp per
+//        embed[ordering[sel[i]*per+j]].x gathered row, bf16 x fp32 in fp32
+//   4. first maximum                     same kernel: 64-bit keys, atomicMax per
+//                                        CTA, the last CTA to finish writes the token
+//
+// Order and ties (the page selects with an unstable partition and scans with a
+// strict '>'): centroids rank by larger logit, NaN last, ties to the lower
+// index, and are visited in that order; among equal scores the first in
+// (rank, position) order wins; NaN and -inf never win, and with no winner the
+// token is 0 and the score -inf.
+#include <math.h>
+
+#include "il_internal.cuh"
+
+namespace il {
+namespace {
+
+constexpr int kTopkThreads = 1024;
+constexpr int kScoreThreads = 256;
+
+// fp32 -> u32 whose unsigned order is the float order (-inf lowest of the numbers).
+__device__ __forceinline__ uint32_t orderable(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_orderable(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+// Larger key = earlier rank: logit first (NaN as the lowest), then lower index.
+// Key 0 is below every centroid (padding of the sort).
+__device__ __forceinline__ unsigned long long rank_key(float v, uint32_t i) {
+  const uint32_t o = isnan(v) ? 0u : orderable(v);
+  return ((unsigned long long)o << 32) | (uint32_t)~i;
+}
+
+// One CTA: sort the rank keys of all n centroids (padded to p, a power of two)
+// in descending order, then write the first k indices.
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ cl, int n, int p, int k,
+                                                            uint32_t* __restrict__ sel) {
+  extern __shared__ unsigned long long keys[];
+  grid_dep_wait();  // cl comes from the previous kernel
+  for (int i = threadIdx.x; i < p; i += blockDim.x) keys[i] = i < n ? rank_key(cl[i], (uint32_t)i) : 0ull;
+  __syncthreads();
+  for (int size = 2; size <= p; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = threadIdx.x; t < (p >> 1); t += blockDim.x) {
+        const int lo = 2 * stride * (t / stride) + (t % stride);
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const unsigned long long a = keys[lo], b = keys[hi];
+        if ((a < b) == desc) {
+          keys[lo] = b;
+          keys[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int r = threadIdx.x; r < k; r += blockDim.x) sel[r] = ~(uint32_t)keys[r];
+  grid_dep_launch();
+}
+
+// Warp per gathered row; x staged once per CTA.  Each CTA folds its best key into
+// *best_key; the last CTA to finish turns it into the token and resets the state.
+__global__ void __launch_bounds__(kScoreThreads) cluster_score_kernel(
+    const float* __restrict__ x, int h, const uint16_t* __restrict__ embed, int64_t row_pitch,
+    const uint32_t* __restrict__ ordering, int64_t vocab, const uint32_t* __restrict__ sel, int k, int per,
+    float* __restrict__ scores_out, unsigned long long* best_key, unsigned* done, uint32_t* __restrict__ token_out,
+    float* __restrict__ score_out, unsigned* status) {
+  extern __shared__ float4 xs4[];
+  __shared__ unsigned long long warp_best[kScoreThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  grid_dep_wait();  // sel comes from the previous kernel
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  for (int i = threadIdx.x; i < h / 4; i += blockDim.x) xs4[i] = x4[i];
+  __syncthreads();
+
+  const int rows = k * per;
+  unsigned long long best = 0ull;
+  for (int row = blockIdx.x * (kScoreThreads / 32) + warp; row < rows; row += gridDim.x * (kScoreThreads / 32)) {
+    const int i = row / per, j = row - (row / per) * per;
+    const uint32_t tok = ordering[(int64_t)sel[i] * per + j];
+    const bool valid = (int64_t)tok < vocab;
+    float acc = 0.f;
+    if (valid) {
+      const uint4* w = reinterpret_cast<const uint4*>(embed + (int64_t)tok * row_pitch);
+#pragma unroll 4
+      for (int e = lane; e < h / 8; e += 32) {
+        const uint4 v = __ldg(w + e);
+        const float4 a = xs4[2 * e], b = xs4[2 * e + 1];
+        acc = fmaf(bf16_lo(v.x), a.x, acc);
+        acc = fmaf(bf16_hi(v.x), a.y, acc);
+        acc = fmaf(bf16_lo(v.y), a.z, acc);
+        acc = fmaf(bf16_hi(v.y), a.w, acc);
+        acc = fmaf(bf16_lo(v.z), b.x, acc);
+        acc = fmaf(bf16_hi(v.z), b.y, acc);
+        acc = fmaf(bf16_lo(v.w), b.z, acc);
+        acc = fmaf(bf16_hi(v.w), b.w, acc);
+      }
+    } else if (lane == 0) {
+      atomicOr(status, kStatusBadToken);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      if (scores_out != nullptr) scores_out[row] = valid ? acc : __int_as_float(0x7fc00000);
+      if (valid && acc > -INFINITY) {  // false for NaN
+        const unsigned long long key = ((unsigned long long)orderable(acc) << 32) | (uint32_t)~(uint32_t)row;
+        best = key > best ? key : best;
+      }
+    }
+  }
+  if (lane == 0) warp_best[warp] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long b = 0ull;
+    for (int w = 0; w < kScoreThreads / 32; ++w) b = warp_best[w] > b ? warp_best[w] : b;
+    if (b != 0ull) atomicMax(best_key, b);
+    __threadfence();
+    const unsigned prev = atomicAdd(done, 1u);
+    if (prev == gridDim.x - 1) {
+      // every other CTA has folded its key in (they fenced before counting)
+      __threadfence();
+      const unsigned long long key = atomicAdd(best_key, 0ull);
+      if (key == 0ull) {
+        *token_out = 0u;
+        if (score_out != nullptr) *score_out = -INFINITY;
+      } else {
+        const int row = (int)~(uint32_t)key;
+        const int i = row / per, j = row - (row / per) * per;
+        *token_out = ordering[(int64_t)sel[i] * per + j];
+        if (score_out != nullptr) *score_out = from_orderable((uint32_t)(key >> 32));
+      }
+      *best_key = 0ull;  // ready for the next call on this stream
+      *done = 0u;
+    }
+  }
+  grid_dep_launch();
+}
+
+}  // namespace
+
+size_t lmhead_topk_smem(int n_cent) {
+  int p = 1;
+  while (p < n_cent) p <<= 1;
+  return (size_t)p * sizeof(unsigned long long);
+}
+
+cudaError_t launch_lmhead(const float* x, int h, const float* cl, int n_cent, int k, const PackedWeight& embed,
+                          const uint32_t* ordering, int per, uint32_t* sel, float* scores_out,
+                          unsigned long long* best_key, unsigned* done, uint32_t* token_out, float* score_out,
+                          unsigned* status, cudaStream_t stream, int num_sms, int* launches) {
+  int p = 1;
+  while (p < n_cent) p <<= 1;
+  const size_t topk_smem = (size_t)p * sizeof(unsigned long long);
+  static unsigned long long attr_set = 0;  // one bit per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !(attr_set & (1ull << dev))) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)lmhead_topk_smem(kMaxCentroids));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(cluster_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(kMaxHeadWidth * sizeof(float)));
+    if (e != cudaSuccess) return e;
+    attr_set |= 1ull << dev;
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = topk_smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = kUsePdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, cl, n_cent, p, k, sel);
+  if (launches) ++*launches;
+  if (e != cudaSuccess) return e;
+
+  const int rows = k * per;
+  const int warps_per_cta = kScoreThreads / 32;
+  int grid = (rows + warps_per_cta - 1) / warps_per_cta;
+  if (grid > 4 * num_sms) grid = 4 * num_sms;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kScoreThreads);
+  cfg.dynamicSmemBytes = (size_t)h * sizeof(float);
+  e = cudaLaunchKernelEx(&cfg, cluster_score_kernel, x, h, reinterpret_cast<const uint16_t*>(embed.quants),
+                         (int64_t)embed.n_in_pad, ordering, (int64_t)embed.n_out, (const uint32_t*)sel, k, per,
+                         scores_out, best_key, done, token_out, score_out, status);
+  if (launches) ++*launches;
+  return e;
+}
+
+}  // namespace il

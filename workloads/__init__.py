@@ -86,6 +86,22 @@ WORKLOADS = (TINY, DECODE_BF16, DECODE_QUANT, PREFILL_BF16, VOCAB, PREFILL_QUANT
 BY_NAME = {w.name: w for w in WORKLOADS}
 
 
+@dataclass(frozen=True)
+class HeadConfig:
+    """A centroid-masked LM head: the vocabulary in n_cent clusters of vocab / n_cent tokens."""
+    name: str
+    h: int
+    vocab: int
+    n_cent: int
+    top_k: int
+    note: str = ""
+
+
+# the dense vocab projection's shape (2560 -> 262144), in 4096 clusters of 64 tokens
+CENTROID_HEAD = HeadConfig("centroid_lm_head", 2560, 262144, 4096, 32,
+                           "top 32 of 4096 clusters scored: 2048 of 262144 vocabulary rows")
+
+
 # ---------------------------------------------------------------------------
 # encodings
 # ---------------------------------------------------------------------------
@@ -204,3 +220,26 @@ def make_workload_batch(workload: Workload, batch: Batch, t: int, fmt: str,
 def make_x(t: int, n_in: int, seed: int) -> np.ndarray:
     g = torch.Generator().manual_seed(seed)
     return torch.randn(t, n_in, generator=g, dtype=torch.float32).numpy().copy()
+
+
+@dataclass
+class HeadInputs:
+    h: int
+    vocab: int
+    n_cent: int
+    x: np.ndarray            # fp32 [h]
+    centroids: np.ndarray    # bf16 host bytes [n_cent][h]
+    embed: np.ndarray        # bf16 host bytes [vocab][h]
+    ordering: np.ndarray     # u32 [vocab], a permutation: cluster c owns [c*per, (c+1)*per)
+
+
+def make_head_inputs(h: int, vocab: int, n_cent: int, seed: int = 0) -> HeadInputs:
+    """x = randn(h), centroids = 0.02*randn(n_cent, h), embed = 0.02*randn(vocab, h) (both
+    rounded to bf16), ordering = a random permutation, all from one seeded generator."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(h, generator=g, dtype=torch.float32)
+    cen = torch.randn(n_cent, h, generator=g, dtype=torch.float32) * W_STD
+    emb = torch.randn(vocab, h, generator=g, dtype=torch.float32) * W_STD
+    order = torch.randperm(vocab, generator=g).numpy().astype(np.uint32)
+    return HeadInputs(h, vocab, n_cent, x.numpy().copy(), encode_bf16(bf16_bits(cen)),
+                      encode_bf16(bf16_bits(emb)), order)
