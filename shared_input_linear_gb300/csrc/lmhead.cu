@@ -23,8 +23,10 @@
 namespace il {
 namespace {
 
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 512;
+constexpr int kSelectMax = 4096;  // larger k sorts every key instead of selecting
 constexpr int kScoreThreads = 256;
+constexpr int kRowVecs = 16;  // rows up to 32 * 16 * 8 = 4096 wide are loaded in one go
 
 // fp32 -> u32 whose unsigned order is the float order (-inf lowest of the numbers).
 __device__ __forceinline__ uint32_t orderable(float v) {
@@ -42,30 +44,114 @@ __device__ __forceinline__ unsigned long long rank_key(float v, uint32_t i) {
   return ((unsigned long long)o << 32) | (uint32_t)~i;
 }
 
-// One CTA: sort the rank keys of all n centroids (padded to p, a power of two)
-// in descending order, then write the first k indices.
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ cl, int n, int p, int k,
-                                                            uint32_t* __restrict__ sel) {
-  extern __shared__ unsigned long long keys[];
-  grid_dep_wait();  // cl comes from the previous kernel
-  for (int i = threadIdx.x; i < p; i += blockDim.x) keys[i] = i < n ? rank_key(cl[i], (uint32_t)i) : 0ull;
-  __syncthreads();
+// Descending bitonic sort of a[0 .. p) in shared memory, p a power of two.
+__device__ void bitonic_desc(unsigned long long* a, int p) {
   for (int size = 2; size <= p; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int t = threadIdx.x; t < (p >> 1); t += blockDim.x) {
         const int lo = 2 * stride * (t / stride) + (t % stride);
         const int hi = lo + stride;
         const bool desc = (lo & size) == 0;
-        const unsigned long long a = keys[lo], b = keys[hi];
-        if ((a < b) == desc) {
-          keys[lo] = b;
-          keys[hi] = a;
+        const unsigned long long x = a[lo], y = a[hi];
+        if ((x < y) == desc) {
+          a[lo] = y;
+          a[hi] = x;
         }
       }
       __syncthreads();
     }
   }
-  for (int r = threadIdx.x; r < k; r += blockDim.x) sel[r] = ~(uint32_t)keys[r];
+}
+
+// One CTA selects the k largest rank keys of the n centroids and writes their
+// indices in rank order.  k <= kSelectMax: a radix select over the 64-bit keys
+// (8-bit digits from the top; the keys are distinct, so the k-th largest is
+// unique) finds the threshold, the k keys at or above it are gathered and only
+// they are sorted.  Larger k: the whole key array (padded to p) is sorted.
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ cl, int n, int p, int k,
+                                                            uint32_t* __restrict__ sel) {
+  extern __shared__ unsigned long long keys[];
+  __shared__ unsigned hist[256];
+  __shared__ unsigned s_bin, s_above, s_count, s_gathered;
+  grid_dep_wait();  // cl comes from the previous kernel
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (k > kSelectMax) {
+    for (int i = threadIdx.x; i < p; i += blockDim.x) keys[i] = i < n ? rank_key(cl[i], (uint32_t)i) : 0ull;
+    __syncthreads();
+    bitonic_desc(keys, p);
+    for (int r = threadIdx.x; r < k; r += blockDim.x) sel[r] = ~(uint32_t)keys[r];
+    grid_dep_launch();
+    return;
+  }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) keys[i] = rank_key(cl[i], (uint32_t)i);
+  unsigned long long prefix = 0ull, mask = 0ull;
+  unsigned remaining = (unsigned)k;  // how many of the keys matching prefix under mask are still to take
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0u;
+    __syncthreads();
+    // most keys share their top bits: lanes with the same bin add once, together
+    for (int base = 0; base < n; base += blockDim.x) {
+      const int i = base + (int)threadIdx.x;
+      const unsigned long long key = i < n ? keys[i] : 0ull;
+      const bool is_cand = i < n && (key & mask) == prefix;
+      const unsigned bin = is_cand ? ((unsigned)(key >> shift) & 255u) : 256u;
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (is_cand && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane L holds bins 8L .. 8L+7; count the candidates in the bins above each
+      unsigned c[8], local = 0u;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        c[q] = hist[lane * 8 + q];
+        local += c[q];
+      }
+      unsigned incl = local;  // candidates in this lane's bins and every higher lane's
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned v = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += v;
+      }
+      unsigned above = incl - local;
+#pragma unroll
+      for (int q = 7; q >= 0; --q) {
+        if (above < remaining && remaining <= above + c[q]) {  // the k-th largest falls in this bin
+          s_bin = (unsigned)(lane * 8 + q);
+          s_above = above;
+          s_count = c[q];
+        }
+        above += c[q];
+      }
+    }
+    __syncthreads();
+    remaining -= s_above;
+    prefix |= (unsigned long long)s_bin << shift;
+    mask |= 255ull << shift;
+    const bool done = s_count == remaining;  // every candidate in the bin is taken
+    __syncthreads();                         // s_* are rewritten by the next round
+    if (done) break;
+  }
+  // gather the k keys whose top bits (under mask) are at least prefix
+  unsigned long long* cand = keys + n;
+  int pk = 1;
+  while (pk < k) pk <<= 1;
+  if (threadIdx.x == 0) s_gathered = 0u;
+  for (int i = threadIdx.x; i < pk; i += blockDim.x) cand[i] = 0ull;
+  __syncthreads();
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + (int)threadIdx.x;
+    const unsigned long long key = i < n ? keys[i] : 0ull;
+    const bool win = i < n && (key & mask) >= prefix;
+    const unsigned ballot = __ballot_sync(0xffffffffu, win);
+    unsigned at = 0u;
+    if (lane == 0 && ballot != 0u) at = atomicAdd(&s_gathered, (unsigned)__popc(ballot));
+    at = __shfl_sync(0xffffffffu, at, 0);
+    if (win) cand[at + __popc(ballot & ((1u << lane) - 1u))] = key;
+  }
+  __syncthreads();
+  bitonic_desc(cand, pk);
+  for (int r = threadIdx.x; r < k; r += blockDim.x) sel[r] = ~(uint32_t)cand[r];
   grid_dep_launch();
 }
 
@@ -93,9 +179,8 @@ __global__ void __launch_bounds__(kScoreThreads) cluster_score_kernel(
     float acc = 0.f;
     if (valid) {
       const uint4* w = reinterpret_cast<const uint4*>(embed + (int64_t)tok * row_pitch);
-#pragma unroll 4
-      for (int e = lane; e < h / 8; e += 32) {
-        const uint4 v = __ldg(w + e);
+      const int nv = h / 8;  // 16-byte vectors in the row
+      auto dot8 = [&](const uint4& v, int e) {
         const float4 a = xs4[2 * e], b = xs4[2 * e + 1];
         acc = fmaf(bf16_lo(v.x), a.x, acc);
         acc = fmaf(bf16_hi(v.x), a.y, acc);
@@ -105,6 +190,19 @@ __global__ void __launch_bounds__(kScoreThreads) cluster_score_kernel(
         acc = fmaf(bf16_hi(v.z), b.y, acc);
         acc = fmaf(bf16_lo(v.w), b.z, acc);
         acc = fmaf(bf16_hi(v.w), b.w, acc);
+      };
+      if (nv <= 32 * kRowVecs) {
+        // the whole row in flight at once: every lane issues all its loads first
+        uint4 v[kRowVecs];
+#pragma unroll
+        for (int m = 0; m < kRowVecs; ++m)
+          if (lane + 32 * m < nv) v[m] = __ldg(w + lane + 32 * m);
+#pragma unroll
+        for (int m = 0; m < kRowVecs; ++m)
+          if (lane + 32 * m < nv) dot8(v[m], lane + 32 * m);
+      } else {
+#pragma unroll 4
+        for (int e = lane; e < nv; e += 32) dot8(__ldg(w + e), e);
       }
     } else if (lane == 0) {
       atomicOr(status, kStatusBadToken);
@@ -149,10 +247,15 @@ __global__ void __launch_bounds__(kScoreThreads) cluster_score_kernel(
 
 }  // namespace
 
-size_t lmhead_topk_smem(int n_cent) {
+// Shared memory of topk_kernel: the sorted key array (padded to a power of two)
+// for k > kSelectMax, else the keys and the gathered winners (padded).
+size_t topk_smem(int n_cent, int k) {
   int p = 1;
   while (p < n_cent) p <<= 1;
-  return (size_t)p * sizeof(unsigned long long);
+  int pk = 1;
+  while (pk < k) pk <<= 1;
+  return k > kSelectMax ? (size_t)p * sizeof(unsigned long long)
+                        : ((size_t)n_cent + (size_t)pk) * sizeof(unsigned long long);
 }
 
 cudaError_t launch_lmhead(const float* x, int h, const float* cl, int n_cent, int k, const PackedWeight& embed,
@@ -161,13 +264,13 @@ cudaError_t launch_lmhead(const float* x, int h, const float* cl, int n_cent, in
                           unsigned* status, cudaStream_t stream, int num_sms, int* launches) {
   int p = 1;
   while (p < n_cent) p <<= 1;
-  const size_t topk_smem = (size_t)p * sizeof(unsigned long long);
   static unsigned long long attr_set = 0;  // one bit per device
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !(attr_set & (1ull << dev))) {
+    // the largest need: kMaxCentroids keys plus kSelectMax winners
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)lmhead_topk_smem(kMaxCentroids));
+                                         (int)topk_smem(kMaxCentroids, kSelectMax));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(cluster_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)(kMaxHeadWidth * sizeof(float)));
@@ -181,7 +284,7 @@ cudaError_t launch_lmhead(const float* x, int h, const float* cl, int n_cent, in
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1);
   cfg.blockDim = dim3(kTopkThreads);
-  cfg.dynamicSmemBytes = topk_smem;
+  cfg.dynamicSmemBytes = topk_smem(n_cent, k);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = kUsePdl ? 1 : 0;
