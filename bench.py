@@ -53,8 +53,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only", default=None, metavar="WORKLOAD:BATCH:FMT:T",
-                    help="time one batch of one workload (e.g. prefill_bf16_gateup_down:gate_up:bf16:512) "
-                         "and print its per-config entry")
+                    help="time one batch of one workload (e.g. prefill_bf16_gateup_down:gate_up:bf16:512), "
+                         "or the centroid LM head (centroid_lm_head), and print its entry")
     return ap.parse_args()
 
 
@@ -512,6 +512,11 @@ def main():
     sil.build()
     sil.load()
     pk = peaks()
+    if args.only == wl.CENTROID_HEAD.name:
+        entry = run_centroid_head(sil, torch, pk)
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "only": entry}))
+        return 0
     if args.only is not None:
         wname, bname, fmt, t = args.only.split(":")
         entries = run_per_config(sil, torch, pk, only=(wname, bname, fmt, int(t)))
