@@ -666,6 +666,14 @@ namespace {
 
 constexpr int kBN = 256;
 
+// Split-K workspace: a fixed block of per-tile arrival counters, then the partial
+// tiles.  The counters must read zero before every launch (the last arriver of
+// each tile puts its counter back); at a fixed size they never share bytes with
+// the partials of any launch, whatever its tile count, and a grown workspace
+// starts zeroed.  Launches with more tiles than counters do not split.
+constexpr int kMaxSplitTiles = 65536;
+constexpr size_t kCounterBytes = (size_t)kMaxSplitTiles * sizeof(unsigned);
+
 struct Plan {
   int splits, kb_per_split, total_tiles;
 };
@@ -684,7 +692,7 @@ Plan plan_launch(int64_t t, int64_t n_in_pad, const GemmJob* jobs, int nj, int n
     sum_n_out += jobs[j].w->n_out;
   }
   pl.kb_per_split = num_kb;
-  if (!allow_split) return pl;
+  if (!allow_split || pl.total_tiles > kMaxSplitTiles) return pl;
   const double flops = 2.0 * (double)t * (double)n_in_pad * (double)sum_n_out;
   const int fmt = jobs[0].w->format;
   const double wbytes = (double)sum_n_out * (double)n_in_pad * (fmt == IL_BF16 ? 2.0 : fmt == IL_Q8 ? 1.125 : 0.625);
@@ -711,7 +719,7 @@ Plan plan_launch(int64_t t, int64_t n_in_pad, const GemmJob* jobs, int nj, int n
   return pl;
 }
 
-size_t counter_bytes(int tiles) { return ((size_t)tiles * sizeof(unsigned) + 255) / 256 * 256; }
+
 
 }  // namespace
 
@@ -721,7 +729,7 @@ size_t gemm_workspace_bytes(int64_t t, int64_t n_in_pad, const GemmJob* jobs, in
     const int nj = n_jobs - j0 < kMaxGemmJobs ? n_jobs - j0 : kMaxGemmJobs;
     const Plan pl = plan_launch(t, n_in_pad, jobs + j0, nj, num_sms, true);
     if (pl.splits > 1) {
-      const size_t b = counter_bytes(pl.total_tiles) + (size_t)pl.total_tiles * pl.splits * kBN * kBM * sizeof(float);
+      const size_t b = kCounterBytes + (size_t)pl.total_tiles * pl.splits * kBN * kBM * sizeof(float);
       if (b > need) need = b;
     }
   }
@@ -777,7 +785,7 @@ cudaError_t launch_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad
   for (int j0 = 0; j0 < n_jobs; j0 += kMaxGemmJobs) {
     const int nj = n_jobs - j0 < kMaxGemmJobs ? n_jobs - j0 : kMaxGemmJobs;
     Plan pl = plan_launch(t, n_in_pad, jobs + j0, nj, num_sms, ws != nullptr);
-    const size_t cbytes = counter_bytes(pl.total_tiles);
+    const size_t cbytes = kCounterBytes;
     if (pl.splits > 1 &&
         cbytes + (size_t)pl.total_tiles * pl.splits * BN * kBM * sizeof(float) > ws_bytes) {
       pl.splits = 1;
@@ -794,7 +802,7 @@ cudaError_t launch_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad
     p.status = status;
     if (pl.splits > 1) {
       // counters are zero when the workspace is created and the last arriver of
-      // every tile puts its counter back to zero
+      // every tile puts its counter back to zero (see kCounterBytes)
       p.counters = static_cast<unsigned*>(ws);
       p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + cbytes);
     }

@@ -99,6 +99,20 @@ def test_tensor_core_shapes(sil, fmt, t, n_in, n_outs):
     assert_parity(b, ys, "tensor-core shapes")
 
 
+def test_stream_k_growing_tile_counts(sil):
+    # consecutive tensor-core batches on one stream whose tile counts grow: the
+    # per-tile arrival counters of the split tiles must start at zero every time
+    import torch
+    s = torch.cuda.Stream()
+    for fmt, t, n_in, n_out in (("bf16", 300, 4096, 128), ("q4", 600, 4096, 1024), ("bf16", 1000, 4096, 4096),
+                                ("q8", 700, 12288, 2048), ("bf16", 64, 8192, 256)):
+        b = wl.make_batch(n_in, (n_out,), t, fmt, seed=t)
+        with torch.cuda.stream(s):
+            ys, guards = run(sil, b, stream=s)
+        assert guards
+        assert_parity_sampled(b, ys, n_samples=128, what=f"{fmt} t={t} n_out={n_out}")
+
+
 def test_bf16_odd_k(sil):
     # bf16 allows any n_in that is a multiple of 8
     for n_in in (8, 40, 264):
