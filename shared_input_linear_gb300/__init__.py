@@ -221,6 +221,23 @@ def matmul_batch_ptr(x_ptr: int, t: int, n_in: int, jobs, stream_ptr: int) -> in
     return _check(load().il_matmul_batch(x_ptr, int(t), int(n_in), arr, len(jobs), stream_ptr))
 
 
+def prepare_jobs(jobs):
+    """A reusable ``il_job`` array for ``[(Weight|handle, n_out, y_ptr)]``: marshal once,
+    call :func:`matmul_batch_prepared` many times."""
+    arr = (_Job * max(1, len(jobs)))()
+    for i, (w, n_out, y) in enumerate(jobs):
+        arr[i].w = w.handle if isinstance(w, Weight) else w
+        arr[i].n_out = int(n_out)
+        arr[i].y = int(y)
+    return arr, len(jobs)
+
+
+def matmul_batch_prepared(x_ptr: int, t: int, n_in: int, prepared, stream_ptr: int) -> int:
+    """``il_matmul_batch`` with a job array from :func:`prepare_jobs`."""
+    arr, n = prepared
+    return _check(load().il_matmul_batch(x_ptr, int(t), int(n_in), arr, n, stream_ptr))
+
+
 def matmul_batch_noalloc_ptr(x_ptr: int, t: int, n_in: int, jobs, stream_ptr: int) -> int:
     """``il_matmul_batch_noalloc`` on raw device pointers (same ``jobs`` form as
     :func:`matmul_batch_ptr`).  The library allocates no device memory for it;
