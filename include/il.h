@@ -107,9 +107,11 @@ il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int
  * All arguments are validated before anything is launched; on any error the
  * call returns a negative il_status with no work enqueued.  On success the
  * work is enqueued asynchronously on `stream`; x, y and the handles must stay
- * valid until it completes.  Tokens t <= 8 run the grouped decode kernel
- * (each weight byte streamed once); larger t cast x to bf16 once and run the
- * tensor-core kernel.  Jobs of different formats in one batch are allowed.
+ * valid until it completes.  Small t runs the grouped decode kernel (each
+ * weight byte streamed once per 8 tokens): t <= 8 for bf16 weights, t <= 16 for
+ * Q8/Q4.  Larger t casts x to bf16 once and runs the tensor-core kernel (Q8/Q4
+ * weights dequantised to bf16 in shared memory, bf16(fp32(d*q))).  Jobs of
+ * different formats in one batch are allowed (one launch per format).
  */
 int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
                     void* stream);
