@@ -537,16 +537,19 @@ __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid
           const int ntok = min(BN, p.t - nt * BN);
 #pragma unroll 1
           for (int c0 = 0; c0 < ntok; c0 += 16) {
-            // 16 tokens at a time: independent loads in flight, slices summed in order
-            // (a partial tile holds every token column, so reads past ntok stay inside it)
-            float v[16];
+            // 16 tokens at a time, both slices' loads issued before any add (the plan
+            // splits at most in two), summed in slice order (a partial tile holds every
+            // token column, so reads past ntok stay inside it)
+            float v[16], w1[16];
+            const float* src0 = base + (size_t)c0 * kBM;
+            const float* src1 = base + ((size_t)BN + c0) * kBM;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = 0.f;
-#pragma unroll 1
-            for (int s = 0; s < p.splits; ++s) {
-              const float* src = base + ((size_t)s * BN + c0) * kBM;
+            for (int j = 0; j < 16; ++j) v[j] = __ldcg(src0 + j * kBM);
+            if (p.splits > 1) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + j * kBM);
+              for (int j = 0; j < 16; ++j) w1[j] = __ldcg(src1 + j * kBM);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += w1[j];
             }
             if (glu) {
               // as in the direct store: the even lane finishes tokens 0..7, the odd 8..15
