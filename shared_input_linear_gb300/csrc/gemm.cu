@@ -261,6 +261,8 @@ __device__ __forceinline__ uint4 dequant_unit(const uint32_t* __restrict__ qw, c
 template <int BN, int FMT>
 __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   constexpr bool kQ = FMT != IL_BF16;
+  // tokens per round of the split-K fixup: 32 where registers allow (bf16: 6 warps)
+  constexpr int kFix = kQ ? 16 : 32;
   constexpr uint32_t kABytes = kBM * kBK * 2;
   constexpr uint32_t kBBytes = BN * kBK * 2;
   constexpr uint32_t kStageBytes = kABytes + kBBytes;
@@ -536,35 +538,35 @@ __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid
           const float* base = p.ws + (size_t)tile * p.splits * (BN * kBM) + lrow;
           const int ntok = min(BN, p.t - nt * BN);
 #pragma unroll 1
-          for (int c0 = 0; c0 < ntok; c0 += 16) {
-            // 16 tokens at a time, both slices' loads issued before any add (the plan
+          for (int c0 = 0; c0 < ntok; c0 += kFix) {
+            // kFix tokens at a time, both slices' loads issued before any add (the plan
             // splits at most in two), summed in slice order (a partial tile holds every
             // token column, so reads past ntok stay inside it)
-            float v[16], w1[16];
+            float v[kFix], w1[kFix];
             const float* src0 = base + (size_t)c0 * kBM;
             const float* src1 = base + ((size_t)BN + c0) * kBM;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = __ldcg(src0 + j * kBM);
+            for (int j = 0; j < kFix; ++j) v[j] = __ldcg(src0 + j * kBM);
             if (p.splits > 1) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) w1[j] = __ldcg(src1 + j * kBM);
+              for (int j = 0; j < kFix; ++j) w1[j] = __ldcg(src1 + j * kBM);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += w1[j];
+              for (int j = 0; j < kFix; ++j) v[j] += w1[j];
             }
             if (glu) {
-              // as in the direct store: the even lane finishes tokens 0..7, the odd 8..15
+              // as in the direct store: the even lane finishes the first half, the odd the second
               const bool odd = lane & 1;
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float keep = odd ? v[j + 8] : v[j];
-                const float got = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + 8], 1);
-                const int c = c0 + j + (odd ? 8 : 0);
+              for (int j = 0; j < kFix / 2; ++j) {
+                const float keep = odd ? v[j + kFix / 2] : v[j];
+                const float got = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + kFix / 2], 1);
+                const int c = c0 + j + (odd ? kFix / 2 : 0);
                 if (row < n_out && c < ntok)
                   y[(int64_t)(nt * BN + c) * (n_out >> 1) + (row >> 1)] = odd ? gelu_mul(got, keep) : gelu_mul(keep, got);
               }
             } else {
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
+              for (int j = 0; j < kFix; ++j)
                 if (c0 + j < ntok) y[(int64_t)(nt * BN + c0 + j) * n_out + row] = v[j];
             }
           }
