@@ -27,6 +27,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 
@@ -617,17 +618,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  // looked up once; a function-local static is initialised thread-safely
+  static const EncodeTiledFn fn = [] {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return static_cast<EncodeTiledFn>(nullptr);
+  }();
   return fn;
 }
 
@@ -778,14 +778,14 @@ cudaError_t launch_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad
   constexpr int BN = kBN;
   constexpr size_t smem = (size_t)kStages * (kBM * kBK * 2 + BN * kBK * 2) +
                           (FMT == IL_BF16 ? 0 : (size_t)kRawStages * kRawStageBytes) + 1024 + 256;
-  static unsigned long long attr_set = 0;  // one bit per device
+  static std::atomic<unsigned long long> attr_set{0};  // one bit per device (setting it twice is harmless)
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !(attr_set & (1ull << dev))) {
+  if (dev >= 64 || !(attr_set.load() & (1ull << dev))) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    attr_set |= 1ull << dev;
+    if (dev < 64) attr_set.fetch_or(1ull << dev);
   }
   for (int j0 = 0; j0 < n_jobs; j0 += kMaxGemmJobs) {
     const int nj = n_jobs - j0 < kMaxGemmJobs ? n_jobs - j0 : kMaxGemmJobs;

@@ -18,6 +18,8 @@
 // token is 0 and the score -inf.
 #include <math.h>
 
+#include <atomic>
+
 #include "il_internal.cuh"
 
 namespace il {
@@ -264,10 +266,10 @@ cudaError_t launch_lmhead(const float* x, int h, const float* cl, int n_cent, in
                           unsigned* status, cudaStream_t stream, int num_sms, int* launches) {
   int p = 1;
   while (p < n_cent) p <<= 1;
-  static unsigned long long attr_set = 0;  // one bit per device
+  static std::atomic<unsigned long long> attr_set{0};  // one bit per device (setting it twice is harmless)
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !(attr_set & (1ull << dev))) {
+  if (dev >= 64 || !(attr_set.load() & (1ull << dev))) {
     // the largest need: kMaxCentroids keys plus kSelectMax winners
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)topk_smem(kMaxCentroids, kSelectMax));
@@ -275,7 +277,7 @@ cudaError_t launch_lmhead(const float* x, int h, const float* cl, int n_cent, in
       e = cudaFuncSetAttribute(cluster_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)(kMaxHeadWidth * sizeof(float)));
     if (e != cudaSuccess) return e;
-    attr_set |= 1ull << dev;
+    if (dev < 64) attr_set.fetch_or(1ull << dev);
   }
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
