@@ -466,6 +466,23 @@ def test_gate_up_check_rule():
     assert not oracle.check_gate_up([np.nan, 0.0, 0.0], g, u, mag_g, mag_u)[0]
 
 
+def test_gate_up_bound_holds_under_sampled_errors():
+    # the derived bar is an upper bound: g and u moved anywhere inside their own bars
+    # (corners included) never move gelu(g)*u by more than gate_up_tolerance
+    rng = np.random.default_rng(7)
+    g = np.concatenate([rng.normal(0, 3, 4000), [0.0, -1.4185, 1.4185, -30.0, 30.0]])
+    u = rng.normal(0, 2, g.size)
+    mag_g = np.abs(g) * rng.uniform(1.0, 5.0, g.size)
+    mag_u = np.abs(u) * rng.uniform(1.0, 5.0, g.size)
+    tol = oracle.gate_up_tolerance(g, u, mag_g, mag_u)
+    h = oracle.gelu_mul(g, u)
+    eg, eu = oracle.tolerance(mag_g), oracle.tolerance(mag_u)
+    for sg, su in [(1, 1), (1, -1), (-1, 1), (-1, -1)] + [(None, None)] * 8:
+        dg = eg * (sg if sg is not None else rng.uniform(-1, 1, g.size))
+        du = eu * (su if su is not None else rng.uniform(-1, 1, g.size))
+        assert np.all(np.abs(oracle.gelu_mul(g + dg, u + du) - h) <= tol)
+
+
 def test_oracle_rejects_bad_format(orc):
     with pytest.raises((ValueError, KeyError)):
         orc.dequant(7, np.zeros(64, np.uint8), 1, 32)
