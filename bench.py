@@ -26,7 +26,6 @@ import re
 import statistics
 import subprocess
 import sys
-import tempfile
 import threading
 import time
 
