@@ -53,7 +53,7 @@ constexpr unsigned long long kWaitLimitCycles = 2ull << 30;  // ~1 s at 2 GHz
 
 constexpr int kMaxGemmJobs = 8;
 
-struct __align__(64) GemmParams {
+struct GemmParams {  // CUtensorMap members give it their 64-byte (or larger) alignment
   CUtensorMap wmap[kMaxGemmJobs];  // bf16: W tiles; Q8/Q4: packed quants, [n_groups][n_chunks * 128] words
   CUtensorMap smap[kMaxGemmJobs];  // Q8/Q4: packed scales, [n_groups][n_chunks * scales_per_chunk] floats
   CUtensorMap xmap;
@@ -73,6 +73,8 @@ struct __align__(64) GemmParams {
   unsigned* status;
   unsigned glu_mask;   // bit j: job j's rows interleave gate/up; y[j] is h = gelu(g) * u, n_out/2 wide
 };
+static_assert(alignof(GemmParams) >= 64, "tensor maps must stay 64-byte aligned in the kernel parameters");
+static_assert(sizeof(GemmParams) <= 4096, "kernel parameters must fit the classic 4 KB limit");
 
 // ---- PTX wrappers -----------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
