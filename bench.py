@@ -210,7 +210,7 @@ def run_headline(sil, torch, args, dist, clocks: ClockSampler):
     # at each graph boundary: that gives the device time of every batch kind
     # over the timed region without events between kernels.
     K = args.steps
-    L = max(d for d in range(1, min(K, 200) + 1) if K % d == 0)
+    L = graph_steps(K)
     graphs = []
     launches_per_rep = 0
     for b in batches:
@@ -467,48 +467,128 @@ def run_dispatch(sil, torch):
 # ---------------------------------------------------------------------------
 # CPU oracle on the host (baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
-def oracle_steps(seconds: float, min_steps: int = 1, max_steps: int | None = None):
+def host_threads() -> int:
+    """Host cores the oracle may use (affinity-aware where the OS says)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
+
+
+def oracle_steps(seconds: float, min_steps: int = 1, max_steps: int | None = None, threads: int = 1):
     import oracle
     inputs = [wl.make_workload_batch(HEADLINE, bt, 1, "bf16") for bt in HEADLINE.batches]
     step_bytes = sum(b.weight_bytes for b in inputs)
-    oracle.matmul_batch(inputs[0].x, inputs[0].jobs[:1])  # load + warm
+    oracle.linear_threads(*inputs[0].jobs[0][:2], inputs[0].jobs[0][2], inputs[0].n_in,
+                          inputs[0].x, threads)  # load + warm
     n, t0 = 0, time.perf_counter()
     while True:
         for b in inputs:
-            oracle.matmul_batch(b.x, b.jobs)
+            for fmt, buf, n_out in b.jobs:
+                oracle.linear_threads(fmt, buf, n_out, b.n_in, b.x, threads)
         n += 1
         el = time.perf_counter() - t0
         if (max_steps is not None and n >= max_steps) or (max_steps is None and n >= min_steps
                                                           and el >= seconds):
             break
-    return {"value": step_bytes / (el / n) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": step_bytes / (el / n) / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} full decode steps (q/k/v + gate/up batches, t=1, bf16 weights, "
-                      f"{step_bytes} weight bytes each), single-threaded C, f64 accumulate",
+                      f"{step_bytes} weight bytes each), C oracle with each job's rows split over "
+                      f"{threads} host threads, f64 accumulate",
             "ms_per_step": el / n * 1e3, "steps": n}
+
+
+def _first_rows(fmt: str, buf: np.ndarray, n_out: int, n_in: int, rows: int) -> np.ndarray:
+    """The first `rows` rows of a weight in its host layout (quants, then scales)."""
+    if fmt == "bf16":
+        return buf[: rows * n_in * 2]
+    qrow = n_in if fmt == "q8" else n_in // 2
+    srow = 4 * (n_in // 32)
+    return np.concatenate([buf[: rows * qrow], buf[n_out * qrow: n_out * qrow + rows * srow]])
+
+
+def oracle_config_ms(inp: wl.BatchInputs, threads: int, budget_macs: float = 1.5e9):
+    """The oracle's time for one whole batch on `threads` host cores, measured on a
+    bounded sample: the first rows of every job (a fraction of each) and, beyond 64
+    tokens, the first 64 token rows; the time is scaled by the work left out (every
+    row and token costs the same)."""
+    import oracle
+    total = float(inp.t) * inp.n_in * sum(n for _, _, n in inp.jobs)
+    x = inp.x[:64]
+    tok_frac = x.shape[0] / inp.t
+    row_frac = min(1.0, budget_macs / (total * tok_frac))
+    done = 0.0
+    t0 = time.perf_counter()
+    for fmt, buf, n_out in inp.jobs:
+        rows = max(1, min(n_out, math.ceil(n_out * row_frac)))
+        oracle.linear_threads(fmt, _first_rows(fmt, buf, n_out, inp.n_in, rows), rows, inp.n_in, x, threads)
+        done += float(x.shape[0]) * inp.n_in * rows
+    el = time.perf_counter() - t0
+    return el * total / done * 1e3, done / total
+
+
+def add_oracle_times(entries, threads: int):
+    """cpu_ms (the oracle on the host cores, per batch) and the GPU's speed-up over it,
+    for every per-config entry."""
+    cache = {}
+    for e in entries:
+        if "error" in e:
+            continue
+        w = wl.BY_NAME[e["workload"]]
+        bt = next(b for b in w.batches if b.name == e["batch"])
+        key = (w.name, bt.name, e["fmt"])
+        if key not in cache:
+            cache.clear()
+            cache[key] = wl.make_workload_batch(w, bt, e["t"], e["fmt"])
+        base = cache[key]
+        inp = wl.BatchInputs(e["fmt"], e["t"], bt.n_in, wl.make_x(e["t"], bt.n_in, seed=0), base.jobs)
+        ms, frac = oracle_config_ms(inp, threads)
+        e["cpu_ms"] = round(ms, 3)
+        e["cpu_cores"] = threads
+        e["cpu_sample_fraction"] = round(frac, 6)
+        e["gpu_speedup_over_cpu"] = round(ms * 1e3 / e["us"], 1)
+
+
+def graph_steps(K: int) -> int:
+    """Launches per captured graph: the largest divisor of K up to 200."""
+    return max(d for d in range(1, min(K, 200) + 1) if K % d == 0)
+
+
+def headline_config(steps: int, world: int) -> dict:
+    """The headline workload's config, the same for both arms of the benchmark."""
+    step_bytes = sum(2 * bt.n_in * sum(bt.n_outs) for bt in HEADLINE.batches)
+    copies = copies_for(step_bytes)
+    return {"workload": "decode_bf16 q/k/v + gate/up batches, t=1, n_in=4096 "
+                        "(n_out 4096+1024+1024 and 12288+12288)",
+            "t": 1, "n_in": 4096, "formats": "bf16",
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": f"weights rotate over {copies} resident copies ({copies * step_bytes / 1e9:.2f} GB > L2)",
+            "timing": f"CUDA graphs of {graph_steps(max(1, steps))} launches replayed, one graph per batch "
+                      "kind, CUDA events at graph boundaries on the launching stream"}
 
 
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    config = {"workload": "decode_bf16 q/k/v + gate/up batches, t=1, n_in=4096 "
-                          "(n_out 4096+1024+1024 and 12288+12288)",
-              "t": 1, "n_in": 4096, "formats": "bf16"}
+    config = headline_config(args.steps, world)
 
     if args.impl == "reference":
         if rank != 0:
             return 0
+        threads = host_threads()
+        # every step is one full decode step: keep K steps of the run bounded
         steps = max(1, args.steps) if args.steps <= 50 else 20
-        warm = min(args.warmup, 2)
+        warm = max(0, args.warmup) if args.warmup <= 50 else 3
         if warm:
-            oracle_steps(0, max_steps=warm)
-        r = oracle_steps(0, max_steps=steps)
+            oracle_steps(0, max_steps=warm, threads=threads)
+        r = oracle_steps(0, max_steps=steps, threads=threads)
         line = {"impl": "reference", "metric": METRIC, "value": round(r["value"], 3),
                 "unit": "GB/s", "n_gpus": args.gpus, "steps": r["steps"], "warmup": warm,
                 "ms_per_step": round(r["ms_per_step"], 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": config,
-                "cpu_baseline": {"value": round(r["value"], 3), "unit": "GB/s", "cores": 1,
+                "cpu_baseline": {"value": round(r["value"], 3), "unit": "GB/s", "cores": r["cores"],
                                  "kind": "oracle", "sample": r["sample"]},
                 "e2e": {"value": round(r["value"], 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
@@ -559,9 +639,12 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r = oracle_steps(args.cpu_seconds)
+        threads = host_threads()
+        r = oracle_steps(args.cpu_seconds, threads=threads)
         cpu = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in r.items()
                if k in ("value", "unit", "cores", "kind", "sample")}
+        if per_config is not None:
+            add_oracle_times(per_config, threads)
 
     if rank == 0:
         kus = head["kernel_us"]
@@ -584,12 +667,7 @@ def main():
                 "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 5),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic (seeded N(0,1) x, N(0,0.02) W)",
-                "config": dict(config, parallelism=f"replicas{world}" if world > 1 else "single",
-                               l2=f"weights rotate over {head['copies']} resident copies "
-                                  f"({head['copies'] * head['step_bytes'] / 1e9:.2f} GB > L2)",
-                               timing=f"CUDA graphs of {head['graph_steps']} launches replayed, "
-                                      "one graph per batch kind, CUDA events at graph boundaries "
-                                      "on the launching stream"),
+                "config": config,
                 "tflops": round(head["step_flops"] * world / (ms * 1e-3) / 1e12, 4),
                 "roofline": roof, "e2e": {k: (round(v, 3) if isinstance(v, float) else v)
                                           for k, v in e2e.items()},

@@ -104,38 +104,54 @@ il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int
  *   jobs   : HOST array of n_jobs il_job (read during the call only).
  *   n_jobs : 0 <= n_jobs <= 4096; 0 is a successful no-op.
  *   stream : cudaStream_t to enqueue on (NULL = legacy default stream).
- * All arguments are validated before anything is launched; on any error the
- * call returns a negative il_status with no work enqueued.  On success the
- * work is enqueued asynchronously on `stream`; x, y and the handles must stay
- * valid until it completes.  Small t runs the grouped decode kernel (each
- * weight byte streamed once per 8 tokens): t <= 8 for bf16 weights, t <= 16 for
- * Q8/Q4.  Larger t casts x to bf16 once and runs the tensor-core kernel (Q8/Q4
- * weights dequantised to bf16 in shared memory, bf16(fp32(d*q))).  Jobs of
- * different formats in one batch are allowed (one launch per format).
+ * All arguments are validated, and every launch of the batch is worked out in
+ * full (plans, tensor maps, scratch), before anything is launched; on any such
+ * error the call returns a negative il_status with no kernel enqueued and no y
+ * written.  Only a launch that the CUDA runtime itself rejects (IL_ERR_CUDA,
+ * "launch") can leave the earlier launches of the batch enqueued.  On success
+ * the work is enqueued asynchronously on `stream`; x, y and the handles must
+ * stay valid until it completes.
+ * Kernels: small t runs the grouped decode kernel, each weight byte streamed
+ * once per 8 tokens: t <= 8 for bf16 weights, t <= 16 for Q8/Q4.  Larger t casts
+ * x to bf16 once and runs the tensor-core kernel (Q8/Q4 weights dequantised to
+ * bf16 in shared memory, bf16(fp32(d*q))).  One launch covers every job of one
+ * format, up to 32 jobs on the decode kernel (per 8 tokens) and 8 jobs on the
+ * tensor-core kernel; a batch beyond those counts, or with several formats,
+ * takes one launch per group.
+ * Scratch: the tensor-core path keeps a bf16 copy of x and a split-K workspace
+ * per (device, stream), owned by the library.  They grow with the stream-ordered
+ * allocator (cudaMallocAsync / cudaFreeAsync on `stream`), so growing never
+ * waits for the stream; they cannot grow while `stream` is being captured
+ * (IL_ERR_UNSUPPORTED): run one call of the largest size on the stream before
+ * capturing it.  il_release_scratch frees them.
  */
 int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
                     void* stream);
 
 /*
  * il_matmul_batch_noalloc -- the pages have no counterpart of this entry point.
- * Same arguments, checks, result and error behaviour as il_matmul_batch, but it
- * never allocates device memory: for callers that cannot let a library call
- * cudaMalloc, such as services that give all device memory to their own pool at
- * start-up, or latency-critical threads for which cudaMalloc / cudaFree may
- * block and synchronise the device.
- *   - The bf16 copy of x used by the tensor-core path (t > 8, bf16 weights)
- *     goes to a fixed 16 MiB device array inside the library, held by every
- *     GPU that loads the library until the process exits.  A batch needing
- *     more, t * round_up(n_in, 128) * 2 bytes > 16 MiB, is rejected with
- *     IL_ERR_UNSUPPORTED (e.g. t = 2048 fits at n_in = 4096, not at 12288).
+ * Same arguments and checks as il_matmul_batch, the same split over the decode
+ * and tensor-core kernels, results equal to il_matmul_batch's within the
+ * per-element tolerance (the tensor-core launches here never split K), and
+ * the same rule that an error enqueues nothing -- but it never allocates
+ * device memory: for callers that cannot let a library call cudaMalloc, such
+ * as services that give all device memory to their own pool at start-up, or
+ * latency-critical threads for which cudaMalloc / cudaFree may block and
+ * synchronise the device.
+ *   - The bf16 copy of x used by the tensor-core path (t >= 9 with bf16
+ *     weights, t >= 17 with Q8/Q4 weights) goes to a fixed 16 MiB device array
+ *     inside the library, held by every GPU that loads the library until the
+ *     process exits.  A batch needing more, t * round_up(n_in, 256) * 2 bytes
+ *     > 16 MiB, is rejected with IL_ERR_UNSUPPORTED (e.g. t = 2048 fits at
+ *     n_in = 4096, not at 12288).
  *   - The first call on a device looks up the array's device address and
- *     clears the library's status word there (a synchronous step); make that
- *     first call before any stream capture.
+ *     clears the library's status word there, asynchronously on `stream`; make
+ *     that first call before any stream capture.
  *   - Every call shares the one array: calls that overlap on the GPU (on
  *     different streams, or from different threads) race and may corrupt each
  *     other's results.  Serialise them, e.g. on one stream.
- *   - A device-side wait of the tensor-core kernel that gives up records its
- *     code in that status word and ends the kernel early.
+ *   - A device-side wait that gives up records its code in that status word
+ *     and ends the kernel early; il_check_device_status reports it.
  */
 int il_matmul_batch_noalloc(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
                             void* stream);
@@ -228,14 +244,21 @@ int il_weight_info(const il_weight* w, int* format, int64_t* n_out, int64_t* n_i
  */
 int il_dequantize_weight(const il_weight* w, float* dev_out, void* stream);
 
-/* Reads (and clears) the device-side status word that bounded waits in the
- * kernels set when they give up.  Synchronises `stream`.  Returns IL_OK, or
- * IL_ERR_DEVICE_TIMEOUT if a wait timed out since the last call; in that case
- * it also clears the library's split-K workspaces on the current device
- * (synchronously), so that later batches start from a clean state.  Returns
- * IL_ERR_ARG if no wait timed out but il_centroid_head met an ordering entry
- * >= vocab. */
+/* Reads (and clears) the device-side status words that bounded waits in the
+ * kernels set when they give up -- the one of il_matmul_batch and
+ * il_centroid_head, and the one of il_matmul_batch_noalloc -- on the current
+ * device.  Synchronises `stream`.  Returns IL_OK, or IL_ERR_DEVICE_TIMEOUT if a
+ * wait timed out since the last call; in that case it also waits for the
+ * device and clears the library's split-K workspaces on it, so that later
+ * batches start from a clean state.  Returns IL_ERR_ARG if no wait timed out
+ * but il_centroid_head met an ordering entry >= vocab. */
 int il_check_device_status(void* stream);
+
+/* Frees the scratch the library keeps for `stream` on the current device (the
+ * bf16 copy of x, the split-K workspace, the LM-head scratch), in stream order:
+ * call it before destroying a stream the library has run on.  A later call on
+ * the stream allocates afresh.  Returns IL_OK or IL_ERR_CUDA. */
+int il_release_scratch(void* stream);
 
 /* Message of the last error on this thread ("" if none). */
 const char* il_last_error(void);

@@ -34,7 +34,9 @@
  * Built with -ffp-contract=off so no multiply-add is fused.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 enum { ORACLE_BF16 = 0, ORACLE_Q8 = 1, ORACLE_Q4 = 2 };
@@ -93,16 +95,14 @@ int oracle_dequant(int format, const void* w, int64_t n_out, int64_t n_in, float
   return 0;
 }
 
-/* One job: y_ref[t][n_out] and mag[t][n_out] in f64 over all tokens.
- * Each weight row is dequantised once into `row` (caller scratch of n_in
+/* Rows [o0, o1) of one job: y_ref[t][n_out] and mag[t][n_out] in f64 over all
+ * tokens.  Each weight row is dequantised once into `row` (scratch of n_in
  * floats); then every token's dot product runs over it with i ascending. */
-int oracle_linear(int format, const void* w, int64_t n_out, int64_t n_in,
-                  const float* x, int64_t t, double* y_ref, double* mag, float* row) {
-  if (format < 0 || format > 2) return -1;
-  if (format != ORACLE_BF16 && n_in % 32 != 0) return -2;
-  for (int64_t o = 0; o < n_out; ++o) {
+static void linear_rows(int format, const uint8_t* w, int64_t n_out, int64_t n_in, const float* x, int64_t t,
+                        int64_t o0, int64_t o1, double* y_ref, double* mag, float* row) {
+  for (int64_t o = o0; o < o1; ++o) {
     for (int64_t i = 0; i < n_in; ++i)
-      row[i] = weight_at(format, (const uint8_t*)w, n_out, n_in, o, i);
+      row[i] = weight_at(format, w, n_out, n_in, o, i);
     for (int64_t tt = 0; tt < t; ++tt) {
       double acc = 0.0, m = 0.0;
       const float* xr = x + tt * n_in;
@@ -115,7 +115,83 @@ int oracle_linear(int format, const void* w, int64_t n_out, int64_t n_in,
       mag[tt * n_out + o] = m;
     }
   }
+}
+
+/* One job over all rows (caller scratch `row` of n_in floats). */
+int oracle_linear(int format, const void* w, int64_t n_out, int64_t n_in,
+                  const float* x, int64_t t, double* y_ref, double* mag, float* row) {
+  if (format < 0 || format > 2) return -1;
+  if (format != ORACLE_BF16 && n_in % 32 != 0) return -2;
+  linear_rows(format, (const uint8_t*)w, n_out, n_in, x, t, 0, n_out, y_ref, mag, row);
   return 0;
+}
+
+/* The same job with its rows split into n_threads contiguous ranges, one POSIX
+ * thread each.  Every element is computed exactly as by oracle_linear (same
+ * dequantisation, same summation order), so the results are identical; only
+ * the wall time differs.  Used to time the oracle on all host cores. */
+struct rows_task {
+  int format;
+  const uint8_t* w;
+  int64_t n_out, n_in, t, o0, o1;
+  const float* x;
+  double *y_ref, *mag;
+  int rc;
+};
+
+static void* rows_thread(void* arg) {
+  struct rows_task* k = (struct rows_task*)arg;
+  float* row = (float*)malloc((size_t)k->n_in * sizeof(float));
+  if (row == NULL) {
+    k->rc = -4;
+    return NULL;
+  }
+  linear_rows(k->format, k->w, k->n_out, k->n_in, k->x, k->t, k->o0, k->o1, k->y_ref, k->mag, row);
+  free(row);
+  k->rc = 0;
+  return NULL;
+}
+
+int oracle_linear_threads(int format, const void* w, int64_t n_out, int64_t n_in, const float* x, int64_t t,
+                          double* y_ref, double* mag, int n_threads) {
+  if (format < 0 || format > 2) return -1;
+  if (format != ORACLE_BF16 && n_in % 32 != 0) return -2;
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 1024) n_threads = 1024;
+  if ((int64_t)n_threads > n_out) n_threads = (int)(n_out > 0 ? n_out : 1);
+  struct rows_task* tasks = (struct rows_task*)calloc((size_t)n_threads, sizeof(struct rows_task));
+  pthread_t* ids = (pthread_t*)calloc((size_t)n_threads, sizeof(pthread_t));
+  int* started = (int*)calloc((size_t)n_threads, sizeof(int));
+  if (tasks == NULL || ids == NULL || started == NULL) {
+    free(tasks);
+    free(ids);
+    free(started);
+    return -4;
+  }
+  int rc = 0;
+  for (int k = 0; k < n_threads; ++k) {
+    tasks[k].format = format;
+    tasks[k].w = (const uint8_t*)w;
+    tasks[k].n_out = n_out;
+    tasks[k].n_in = n_in;
+    tasks[k].t = t;
+    tasks[k].o0 = n_out * k / n_threads;
+    tasks[k].o1 = n_out * (k + 1) / n_threads;
+    tasks[k].x = x;
+    tasks[k].y_ref = y_ref;
+    tasks[k].mag = mag;
+    tasks[k].rc = -5;
+    started[k] = pthread_create(&ids[k], NULL, rows_thread, &tasks[k]) == 0;
+    if (!started[k]) rows_thread(&tasks[k]);  /* no thread: run the range here */
+  }
+  for (int k = 0; k < n_threads; ++k) {
+    if (started[k]) pthread_join(ids[k], NULL);
+    if (tasks[k].rc != 0) rc = tasks[k].rc;
+  }
+  free(tasks);
+  free(ids);
+  free(started);
+  return rc;
 }
 
 /* Sampled outputs: for each s, the single element (tok[s], row[s]) of one job,

@@ -19,7 +19,7 @@ import numpy as np
 
 __all__ = ["ILError", "Weight", "FORMATS", "IL_BF16", "IL_Q8", "IL_Q4", "load", "build",
            "upload_weight", "matmul_batch", "matmul_batch_ptr", "matmul_batch_noalloc_ptr", "free_weight", "weight_bytes",
-           "dequantize_weight", "check_device_status", "get_stats", "reset_stats", "last_error",
+           "dequantize_weight", "check_device_status", "release_scratch", "get_stats", "reset_stats", "last_error",
            "version", "LIB_PATH", "STATUS"]
 
 IL_BF16, IL_Q8, IL_Q4 = 0, 1, 2
@@ -94,6 +94,8 @@ def load() -> ctypes.CDLL:
         lib.il_dequantize_weight.restype = ci
         lib.il_check_device_status.argtypes = [vp]
         lib.il_check_device_status.restype = ci
+        lib.il_release_scratch.argtypes = [vp]
+        lib.il_release_scratch.restype = ci
         lib.il_last_error.argtypes = []
         lib.il_last_error.restype = ctypes.c_char_p
         lib.il_last_status.argtypes = []
@@ -276,6 +278,11 @@ def dequantize_weight(w: Weight, out, stream=None) -> None:
 
 def check_device_status(stream=None) -> None:
     _check(load().il_check_device_status(_stream_ptr(stream)))
+
+
+def release_scratch(stream=None) -> None:
+    """``il_release_scratch``: frees the library's scratch for ``stream`` (stream-ordered)."""
+    _check(load().il_release_scratch(_stream_ptr(stream)))
 
 
 def get_stats() -> dict:

@@ -32,6 +32,7 @@
 #include <cstring>
 
 #include "il_internal.cuh"
+#include "il_ptx.cuh"
 
 namespace il {
 namespace {
@@ -49,13 +50,12 @@ constexpr uint32_t kRawStageBytes = kRawQuantBytes + 16 * 8 * 4 * 4;  // + scale
 __host__ __device__ constexpr int gemm_threads(int fmt) { return fmt == IL_BF16 ? kThreadsGemm : kThreadsQ; }
 // fp32 scales per (row group, chunk): 8 rows x the chunk's 32-blocks
 __host__ __device__ constexpr int scales_per_chunk(int fmt) { return 8 * blocks_per_chunk(fmt); }
-constexpr unsigned long long kWaitLimitCycles = 2ull << 30;  // ~1 s at 2 GHz
 
 constexpr int kMaxGemmJobs = 8;
 
 struct GemmParams {  // CUtensorMap members give it their 64-byte (or larger) alignment
-  CUtensorMap wmap[kMaxGemmJobs];  // bf16: W tiles; Q8/Q4: packed quants, [n_groups][n_chunks * 128] words
-  CUtensorMap smap[kMaxGemmJobs];  // Q8/Q4: packed scales, [n_groups][n_chunks * scales_per_chunk] floats
+  CUtensorMap wmap[kMaxGemmJobs];  // bf16: W tiles; Q8/Q4: packed quants, 4D over the records (see make_quant_map)
+  CUtensorMap smap[kMaxGemmJobs];  // Q8/Q4: packed scales, 4D over the records
   CUtensorMap xmap;
   float* y[kMaxGemmJobs];
   int n_out[kMaxGemmJobs];
@@ -76,65 +76,7 @@ struct GemmParams {  // CUtensorMap members give it their 64-byte (or larger) al
 static_assert(alignof(GemmParams) >= 64, "tensor maps must stay 64-byte aligned in the kernel parameters");
 static_assert(sizeof(GemmParams) <= 4096, "kernel parameters must fit the classic 4 KB limit");
 
-// ---- PTX wrappers -----------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n"
-      ".reg .pred P1;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n"
-      "selp.b32 %0, 1, 0, P1;\n"
-      "}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait: false (and the abort flag raised, the code recorded) on timeout
-// or when another role has already aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                         unsigned* status, unsigned code) {
-  const long long start = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    // a phase that completed stays completed: re-check so that roles waiting on
-    // the same phase agree even when the abort flag rises meanwhile
-    if (*abort_flag) return mbar_try_wait(bar, parity);
-    if ((unsigned long long)(clock64() - start) > kWaitLimitCycles) {
-      *abort_flag = 1;
-      atomicOr(status, code);
-      return false;
-    }
-  }
-  return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                           uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
+// ---- PTX wrappers (tcgen05) ---------------------------------------------------
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -344,8 +286,9 @@ __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid
             mbar_expect_tx(rb, kRawTx);
             const uint32_t r_dst = smem_u32(raw + rstage * kRawStageBytes);
             const int c = kb / kKbPerRaw;
-            tma_load_2d(r_dst, wm, c * 128, mt * 16, rb);
-            tma_load_2d(r_dst + kRawQuantBytes, &p.smap[job], c * scales_per_chunk(FMT), mt * 16, rb);
+            // 8 row pairs (16 groups) of chunk c: [pair][group][words] = 16 groups x 512 bytes
+            tma_load_4d(r_dst, wm, 0, 0, c, mt * 8, rb);
+            tma_load_4d(r_dst + kRawQuantBytes, &p.smap[job], 0, 0, c, mt * 8, rb);
             if (++rstage == kRawStages) {
               rstage = 0;
               rphase ^= 1;
@@ -633,11 +576,21 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Host-side fault injection for the failure tests: with
+// IL_FAULT_TENSOR_MAP_FAIL_AFTER=k the (k+1)-th tensor-map encoding of the
+// process fails (as an encoding the driver rejects would).
+std::atomic<long> g_map_count{0};
+bool map_fault() {
+  const char* env = getenv("IL_FAULT_TENSOR_MAP_FAIL_AFTER");
+  if (env == nullptr || *env == '\0') return false;
+  return g_map_count.fetch_add(1) >= strtol(env, nullptr, 10);
+}
+
 // bf16 [rows][cols] row-major with row pitch `pitch` elements; box = box_cols x box_rows.
 bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch, uint32_t box_cols,
               uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
+  if (fn == nullptr || map_fault()) return false;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {pitch * 2};
   const cuuint32_t box[2] = {box_cols, box_rows};
@@ -655,18 +608,15 @@ int grid_cast(int64_t work) {
 
 }  // namespace
 
-cudaError_t launch_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_in_pad, __nv_bfloat16* out,
-                             cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(grid_cast(t * (n_in_pad / 8)));
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = kUsePdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, cast_bf16_kernel, x, t, n_in, n_in_pad, out);
+cudaError_t prepare_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_in_pad, __nv_bfloat16* out,
+                              Launch* L) {
+  *L = Launch();
+  L->fn = reinterpret_cast<const void*>(cast_bf16_kernel);
+  L->grid = dim3(grid_cast(t * (n_in_pad / 8)));
+  L->block = dim3(256);
+  if (kUsePdl) L->allow_early_start();
+  if (!L->set_args(x, t, n_in, n_in_pad, out)) return cudaErrorMemoryAllocation;
+  return cudaSuccess;
 }
 
 namespace {
@@ -678,8 +628,8 @@ constexpr int kBN = 256;
 // each tile puts its counter back); at a fixed size they never share bytes with
 // the partials of any launch, whatever its tile count, and a grown workspace
 // starts zeroed.  Launches with more tiles than counters do not split.
-constexpr int kMaxSplitTiles = 65536;
-constexpr size_t kCounterBytes = (size_t)kMaxSplitTiles * sizeof(unsigned);
+constexpr int kMaxSplitTiles = kSplitCounters;
+constexpr size_t kCounterBytes = kSplitCounterBytes;
 
 struct Plan {
   int splits, kb_per_split, total_tiles;
@@ -745,38 +695,42 @@ size_t gemm_workspace_bytes(int64_t t, int64_t n_in_pad, const GemmJob* jobs, in
 
 namespace {
 
-// Packed Q8/Q4 quants as a 2D tensor of 32-bit words: one row per row group
-// (all its chunks back to back, 512 bytes each); box = one chunk x 16 groups.
+// Packed Q8/Q4 records (il_internal.cuh) seen as 4D tensors.  Quants: 32-bit
+// words, dims {128 words of a group's chunk, 2 groups of a pair, n_chunks,
+// n_pairs}; a box of {128, 2, 1, 8} is one chunk of 16 groups (128 rows), laid
+// out in shared memory as [group][128 words].  Scales: fp32, dims {8 rows x
+// blocks, 2 groups, n_chunks, n_pairs} starting 1024 bytes into the first
+// record; box {8 * blocks, 2, 1, 8} gives [group][rows x blocks].
 bool make_quant_map(CUtensorMap* m, const PackedWeight& w) {
   EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)w.n_chunks * 128, (cuuint64_t)w.n_groups};
-  const cuuint64_t strides[1] = {(cuuint64_t)w.n_chunks * 512};
-  const cuuint32_t box[2] = {128, 16};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, w.quants, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  if (fn == nullptr || map_fault()) return false;
+  const cuuint64_t rs = (cuuint64_t)record_bytes(w.format);
+  const cuuint64_t dims[4] = {128, 2, (cuuint64_t)w.n_chunks, (cuuint64_t)(w.n_groups / 2)};
+  const cuuint64_t strides[3] = {512, rs, rs * (cuuint64_t)w.n_chunks};
+  const cuuint32_t box[4] = {128, 2, 1, 8};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, w.quants, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Packed scales: one row per row group, scales_per_chunk floats per chunk.
 bool make_scale_map(CUtensorMap* m, const PackedWeight& w) {
   EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
+  if (fn == nullptr || map_fault()) return false;
   const int spc = scales_per_chunk(w.format);
-  const cuuint64_t dims[2] = {(cuuint64_t)w.n_chunks * spc, (cuuint64_t)w.n_groups};
-  const cuuint64_t strides[1] = {(cuuint64_t)w.n_chunks * spc * 4};
-  const cuuint32_t box[2] = {(cuuint32_t)spc, 16};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, w.scales, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const cuuint64_t rs = (cuuint64_t)record_bytes(w.format);
+  const cuuint64_t dims[4] = {(cuuint64_t)spc, 2, (cuuint64_t)w.n_chunks, (cuuint64_t)(w.n_groups / 2)};
+  const cuuint64_t strides[3] = {(cuuint64_t)chunk_scale_bytes(w.format), rs, rs * (cuuint64_t)w.n_chunks};
+  const cuuint32_t box[4] = {(cuuint32_t)spc, 2, 1, 8};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, w.quants + 2 * kChunkBytes, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int FMT>
-cudaError_t launch_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs, int n_jobs,
-                            cudaStream_t stream, int num_sms, unsigned* status, int* launches, void* ws,
-                            size_t ws_bytes) {
+cudaError_t prepare_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs, int n_jobs,
+                             int num_sms, unsigned* status, void* ws, size_t ws_bytes, std::vector<Launch>* out) {
   constexpr int BN = kBN;
   constexpr size_t smem = (size_t)kStages * (kBM * kBK * 2 + BN * kBK * 2) +
                           (FMT == IL_BF16 ? 0 : (size_t)kRawStages * kRawStageBytes) + 1024 + 256;
@@ -838,35 +792,29 @@ cudaError_t launch_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad
     p.tile_begin[nj] = tiles;
     p.total_tiles = tiles;
     const int units = tiles * p.splits;
-    const int grid = units < num_sms ? units : num_sms;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(gemm_threads(FMT));
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = kUsePdl ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, FMT>, p);
-    if (launches) ++*launches;
-    if (e != cudaSuccess) return e;
+    Launch L;
+    L.fn = reinterpret_cast<const void*>(gemm_kernel<BN, FMT>);
+    L.grid = dim3(units < num_sms ? units : num_sms);
+    L.block = dim3(gemm_threads(FMT));
+    L.smem = smem;
+    if (kUsePdl) L.allow_early_start();
+    if (!L.set_args(p)) return cudaErrorMemoryAllocation;
+    out->push_back(L);
   }
   return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(int fmt, const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs,
-                        int n_jobs, cudaStream_t stream, int num_sms, unsigned* status, int* launches, void* ws,
-                        size_t ws_bytes) {
+cudaError_t prepare_gemm(int fmt, const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs,
+                         int n_jobs, int num_sms, unsigned* status, void* ws, size_t ws_bytes,
+                         std::vector<Launch>* out) {
   if (fmt == IL_BF16)
-    return launch_gemm_fmt<IL_BF16>(xb, t, n_in_pad, jobs, n_jobs, stream, num_sms, status, launches, ws, ws_bytes);
+    return prepare_gemm_fmt<IL_BF16>(xb, t, n_in_pad, jobs, n_jobs, num_sms, status, ws, ws_bytes, out);
   if (fmt == IL_Q8)
-    return launch_gemm_fmt<IL_Q8>(xb, t, n_in_pad, jobs, n_jobs, stream, num_sms, status, launches, ws, ws_bytes);
+    return prepare_gemm_fmt<IL_Q8>(xb, t, n_in_pad, jobs, n_jobs, num_sms, status, ws, ws_bytes, out);
   if (fmt == IL_Q4)
-    return launch_gemm_fmt<IL_Q4>(xb, t, n_in_pad, jobs, n_jobs, stream, num_sms, status, launches, ws, ws_bytes);
+    return prepare_gemm_fmt<IL_Q4>(xb, t, n_in_pad, jobs, n_jobs, num_sms, status, ws, ws_bytes, out);
   return cudaErrorInvalidValue;
 }
 

@@ -1,4 +1,5 @@
-// gemv.cu -- grouped decode kernel for small token counts (t <= 8).
+// gemv.cu -- grouped decode kernel for bf16 weights at small token counts (t <= 8);
+// Q8 / Q4 weights run the shared-memory ring kernel of qdecode.cu.
 //
 // Computes, for every job j of a batch over one shared x (oxinfer src/gpu.rs,
 // struct `Job` and `Backend::matmul`):   y_j[t][o] = sum_i x[t][i] * w_j[o][i].
@@ -13,10 +14,6 @@
 //    operand (8 rows), and the "A" operand holds 8 tokens of x split into a
 //    bf16 high part (rows 0-7) and the bf16 rounding of the remainder (rows
 //    8-15), so x keeps ~16 significant bits and one MMA serves any t <= 8.
-//    Q8 / Q4 weights are turned into exact fp16 integers in registers and meet
-//    an fp16 hi/lo split of x scaled by a power of two per CTA (so no value of
-//    x overflows fp16); the fp32 scale of each 32-block multiplies the fp32
-//    partial of that block, and the power of two is undone in the epilogue.
 //  * x is staged once per CTA in shared memory, already in MMA fragment
 //    order.  When x's K range is large or the batch has few rows, K is split
 //    over the CTAs of a thread-block cluster, whose partial sums are reduced
@@ -52,22 +49,6 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint4& a, uint32_t
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
-}
-
-// (hi pair, lo pair) of two fp32 values in fp16: hi = f16_rn(v), lo = f16_rn(v - hi).
-__device__ __forceinline__ void split_pair_f16(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(a, b);
-  const float2 hf = __half22float2(h);
-  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
 // (hi pair, lo pair) of two fp32 values: hi = bf16_rn(v), lo = bf16_rn(v - hi).
 __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -77,12 +58,8 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-template <int FMT>
-struct Fmt {
-  static constexpr int CK = chunk_k(FMT);       // columns per chunk
-  static constexpr int SPC = CK / 16;           // MMA slots per chunk
-  static constexpr int SV = FMT == IL_BF16 ? 0 : (FMT == IL_Q8 ? 1 : 2);  // uint4 of scales
-};
+constexpr int kChunkK = 32;   // bf16 columns per chunk (two MMA slots)
+constexpr int kSlotsPerChunk = 2;
 
 __device__ __forceinline__ int find_job(const DecodeParams& p, int gidx) {
   int j = p.n_jobs - 1;
@@ -90,14 +67,10 @@ __device__ __forceinline__ int find_job(const DecodeParams& p, int gidx) {
   return j;
 }
 
-template <int FMT, int G, int B, bool CLUSTER>
+template <int G, int B, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
-  using F = Fmt<FMT>;
   constexpr int GPB = kWarps * G;
-  constexpr int SVN = F::SV > 0 ? F::SV : 1;
-  constexpr int kWStep = FMT == IL_BF16 ? 64 : 512;  // bytes per chunk along a lane's stream
-  constexpr int kSStep = 16 * SVN;                   // floats per chunk along a q's scale stream
-  constexpr int NA = FMT == IL_BF16 ? 2 : 1;         // accumulator sets per group (independent MMA chains)
+  constexpr int kWStep = 64;  // bytes per chunk along a lane's stream (32 columns of bf16)
   extern __shared__ __align__(16) uint8_t smem[];
 
   const int lane = threadIdx.x & 31;
@@ -116,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
   const int nb = c_cnt / B;                                          // batches per row block
   const int my_rbs = (p.n_rowblocks - cid + nclusters - 1) / nclusters;
   const int total = my_rbs * nb;                                     // batches of this warp
-  const int slots = p.chunks_per_slice * F::SPC;
+  const int slots = p.chunks_per_slice * kSlotsPerChunk;
   uint4* xf = reinterpret_cast<uint4*>(smem);
   float* red = reinterpret_cast<float*>(smem + (size_t)slots * 512);
 
@@ -125,7 +98,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
   // group 0 instead: its results are never stored, and the loads stay
   // branch-free.
   const uint8_t* lw[G];
-  const float* ls[G];
   auto set_load_rb = [&](int rbi) {
     const int rb = cid + rbi * nclusters;
 #pragma unroll
@@ -134,12 +106,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
       if (gidx >= p.total_groups) gidx = 0;
       const DecodeJob& jb = p.jobs[find_job(p, gidx)];
       const int64_t lg = gidx - jb.group_begin;
-      if (FMT == IL_BF16) {
-        lw[g] = jb.w + ((lg * 8 + n) * jb.row_stride + (int64_t)c_begin * 32 + 8 * q) * 2;
-      } else {
-        lw[g] = jb.w + ((lg * jb.row_stride + c_begin) * 32 + lane) * 16;
-        ls[g] = jb.s + ((lg * jb.row_stride + c_begin) * 4 + q) * (4 * F::SV);
-      }
+      lw[g] = jb.w + ((lg * 8 + n) * jb.row_stride + (int64_t)c_begin * kChunkK + 8 * q) * 2;
     }
   };
   // Loads move in batches of B consecutive chunks per group, double buffered:
@@ -147,18 +114,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
   // always in flight while the other is consumed.
   int l_rb = 0, l_b = 0;
   set_load_rb(0);
-  auto load_batch = [&](uint4 (&dq)[B][G], uint4 (&ds)[B][G][SVN]) {
+  auto load_batch = [&](uint4 (&dq)[B][G]) {
 #pragma unroll
     for (int i = 0; i < B; ++i)
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        dq[i][g] = __ldg(reinterpret_cast<const uint4*>(lw[g] + (l_b * B + i) * kWStep));
-        if (F::SV > 0) {
-#pragma unroll
-          for (int v = 0; v < F::SV; ++v)
-            ds[i][g][v] = __ldg(reinterpret_cast<const uint4*>(ls[g] + (l_b * B + i) * kSStep) + v);
-        }
-      }
+      for (int g = 0; g < G; ++g) dq[i][g] = __ldg(reinterpret_cast<const uint4*>(lw[g] + (l_b * B + i) * kWStep));
     if (++l_b == nb) {
       l_b = 0;
       set_load_rb(++l_rb);
@@ -166,74 +126,35 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
   };
 
   uint4 qa[B][G], qb[B][G];
-  uint4 sa[B][G][SVN], sb[B][G][SVN];
   // Start the weight stream before staging x so HBM is busy from the first cycle;
   // the weights do not depend on the previous kernel, x may.
-  if (total > 0) load_batch(qa, sa);
-  if (total > 1) load_batch(qb, sb);
+  if (total > 0) load_batch(qa);
+  if (total > 1) load_batch(qb);
   grid_dep_wait();
+  // the next kernel may now be scheduled; it waits for this one before touching x or y
+  grid_dep_launch();
 
   // ---- stage this CTA's K slice of x in fragment order (hi/lo split)
-  auto x_col = [&](int e, int& m, int& k) -> bool {
-    const int s = e >> 5, L = e & 31, qq = L & 3;
-    m = L >> 2;
-    if (FMT == IL_BF16)
-      k = 32 * (c_begin + (s >> 1)) + 8 * qq + 4 * (s & 1);
-    else
-      k = F::CK * c_begin + 16 * s + 4 * qq;
-    return m < p.t && k < p.n_in && s < c_cnt * F::SPC;
-  };
-  // Q8/Q4 (fp16 path): scale each token's x by 2^-x_exp so that its largest |x| in
-  // this slice lies in [2^13, 2^14), well inside fp16's range; the epilogue
-  // multiplies by 2^x_exp.  The scale is per token, so a token's precision does not
-  // depend on the magnitudes of the others.  x_exp stays in [-126, 114]: both powers
-  // of two are normal floats and even |x| near FLT_MAX (ilogb 127) lands in range.
-  // A thread's staging elements e all have e % 32 == lane, so it only ever sees
-  // token n = lane / 4: the max reduces over the four lanes q of that token.
-  int x_exp = 0;
-  if (FMT != IL_BF16) {
-    __shared__ unsigned s_max_bits[8];
-    if (threadIdx.x < 8) s_max_bits[threadIdx.x] = 0u;
-    __syncthreads();
-    float mx = 0.f;
-    for (int e = threadIdx.x; e < slots * 32; e += kThreads) {
-      int m, k;
-      if (x_col(e, m, k)) {
-        const float4 xv = *reinterpret_cast<const float4*>(p.x + (int64_t)m * p.x_row_stride + k);
-        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(xv.x), fabsf(xv.y)), fmaxf(fabsf(xv.z), fabsf(xv.w))));
-      }
-    }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    if (q == 0 && mx > 0.f) atomicMax(&s_max_bits[n], __float_as_uint(mx));  // non-negative: bits order as values
-    __syncthreads();
-    const float smax = __uint_as_float(s_max_bits[n]);
-    x_exp = smax > 0.f ? max(-126, min(114, ilogbf(smax) - 13)) : 0;
-  }
-  const float x_scale = ldexpf(1.0f, -x_exp);
   for (int e = threadIdx.x; e < slots * 32; e += kThreads) {
-    int m, k;
+    const int sl = e >> 5, L = e & 31, qq = L & 3;
+    const int m = L >> 2;
+    const int k = kChunkK * (c_begin + (sl >> 1)) + 8 * qq + 4 * (sl & 1);
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (x_col(e, m, k)) {
+    if (m < p.t && k < p.n_in && sl < c_cnt * kSlotsPerChunk) {
       const float4 xv = *reinterpret_cast<const float4*>(p.x + (int64_t)m * p.x_row_stride + k);
-      if (FMT == IL_BF16) {
-        split_pair(xv.x, xv.y, v.x, v.y);
-        split_pair(xv.z, xv.w, v.z, v.w);
-      } else {
-        split_pair_f16(xv.x * x_scale, xv.y * x_scale, v.x, v.y);
-        split_pair_f16(xv.z * x_scale, xv.w * x_scale, v.z, v.w);
-      }
+      split_pair(xv.x, xv.y, v.x, v.y);
+      split_pair(xv.z, xv.w, v.z, v.w);
     }
     xf[e] = v;
   }
   __syncthreads();
-  const float y_scale = ldexpf(1.0f, x_exp);
 
-  float acc[G][NA][4];
+  // two accumulator sets per group: independent MMA chains
+  float acc[G][2][4];
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int a = 0; a < NA; ++a) acc[g][a][0] = acc[g][a][1] = acc[g][a][2] = acc[g][a][3] = 0.f;
+    for (int a = 0; a < 2; ++a) acc[g][a][0] = acc[g][a][1] = acc[g][a][2] = acc[g][a][3] = 0.f;
 
   int c_rb = 0, c_b = 0;  // consume cursor
   auto epilogue = [&]() {
@@ -243,13 +164,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
     for (int g = 0; g < G; ++g) {
       float r[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int a = 0; a < NA; ++a) {
+      for (int a = 0; a < 2; ++a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) r[j] += acc[g][a][j];
         acc[g][a][0] = acc[g][a][1] = acc[g][a][2] = acc[g][a][3] = 0.f;
       }
-      v[g][0] = (r[0] + r[2]) * y_scale;  // token n, row 2q   (hi + lo parts of x)
-      v[g][1] = (r[1] + r[3]) * y_scale;  // token n, row 2q+1
+      v[g][0] = r[0] + r[2];  // token n, row 2q   (hi + lo parts of x)
+      v[g][1] = r[1] + r[3];  // token n, row 2q+1
     }
     if (!CLUSTER) {
 #pragma unroll
@@ -302,67 +223,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
     }
   };
 
-  auto consume = [&](const uint4 (&cq)[B][G], const uint4 (&cs)[B][G][SVN]) {
-    const uint4* xb = xf + (c_b * B * F::SPC) * 32 + lane;
+  auto consume = [&](const uint4 (&cq)[B][G]) {
+    const uint4* xb = xf + (c_b * B * kSlotsPerChunk) * 32 + lane;
 #pragma unroll
     for (int i = 0; i < B; ++i) {
-      const uint4* xs = xb + (i * F::SPC) * 32;
-      if (FMT == IL_BF16) {
-        const uint4 a0 = xs[0], a1 = xs[32];
+      const uint4* xs = xb + (i * kSlotsPerChunk) * 32;
+      const uint4 a0 = xs[0], a1 = xs[32];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          mma_bf16(acc[g][0], a0, cq[i][g].x, cq[i][g].y);
-          mma_bf16(acc[g][NA - 1], a1, cq[i][g].z, cq[i][g].w);
-        }
-      } else if (FMT == IL_Q8) {
-        // two independent 32-blocks: both first MMAs, then both second MMAs
-        const uint4 a0 = xs[0], a1 = xs[32], a2 = xs[64], a3 = xs[96];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float t4[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-          uint32_t bq[4][2];
-          q8_word_to_f16x2(cq[i][g].x, bq[0][0], bq[0][1]);
-          q8_word_to_f16x2(cq[i][g].y, bq[1][0], bq[1][1]);
-          q8_word_to_f16x2(cq[i][g].z, bq[2][0], bq[2][1]);
-          q8_word_to_f16x2(cq[i][g].w, bq[3][0], bq[3][1]);
-          mma_f16(t4[0], a0, bq[0][0], bq[0][1]);
-          mma_f16(t4[1], a2, bq[2][0], bq[2][1]);
-          mma_f16(t4[0], a1, bq[1][0], bq[1][1]);
-          mma_f16(t4[1], a3, bq[3][0], bq[3][1]);
-          float* ac = acc[g][0];
-          const float d00 = __uint_as_float(cs[i][g][0].x), d01 = __uint_as_float(cs[i][g][0].y);  // row 2q
-          const float d10 = __uint_as_float(cs[i][g][0].z), d11 = __uint_as_float(cs[i][g][0].w);  // row 2q+1
-          ac[0] = fmaf(d00, t4[0][0], ac[0]);
-          ac[2] = fmaf(d00, t4[0][2], ac[2]);
-          ac[1] = fmaf(d10, t4[0][1], ac[1]);
-          ac[3] = fmaf(d10, t4[0][3], ac[3]);
-          ac[0] = fmaf(d01, t4[1][0], ac[0]);
-          ac[2] = fmaf(d01, t4[1][2], ac[2]);
-          ac[1] = fmaf(d11, t4[1][1], ac[1]);
-          ac[3] = fmaf(d11, t4[1][3], ac[3]);
-        }
-      } else {
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {  // one 32-block per word
-          const uint4 a0 = xs[(2 * w) * 32], a1 = xs[(2 * w + 1) * 32];
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const uint32_t word = w == 0 ? cq[i][g].x : (w == 1 ? cq[i][g].y : (w == 2 ? cq[i][g].z : cq[i][g].w));
-            float t4[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pr[4];
-            q4_word_to_f16x2(word, pr);
-            mma_f16(t4, a0, pr[0], pr[1]);
-            mma_f16(t4, a1, pr[2], pr[3]);
-            const uint4 s0 = cs[i][g][0], s1 = cs[i][g][SVN - 1];
-            const float d0 = __uint_as_float(w == 0 ? s0.x : (w == 1 ? s0.y : (w == 2 ? s0.z : s0.w)));
-            const float d1 = __uint_as_float(w == 0 ? s1.x : (w == 1 ? s1.y : (w == 2 ? s1.z : s1.w)));
-            float* ac = acc[g][0];
-            ac[0] = fmaf(d0, t4[0], ac[0]);
-            ac[2] = fmaf(d0, t4[2], ac[2]);
-            ac[1] = fmaf(d1, t4[1], ac[1]);
-            ac[3] = fmaf(d1, t4[3], ac[3]);
-          }
-        }
+      for (int g = 0; g < G; ++g) {
+        mma_bf16(acc[g][0], a0, cq[i][g].x, cq[i][g].y);
+        mma_bf16(acc[g][1], a1, cq[i][g].z, cq[i][g].w);
       }
     }
     if (++c_b == nb) {
@@ -373,15 +243,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
   };
 
   for (int bi = 0; bi < total; bi += 2) {
-    consume(qa, sa);
-    if (bi + 2 < total) load_batch(qa, sa);
+    consume(qa);
+    if (bi + 2 < total) load_batch(qa);
     if (bi + 1 < total) {
-      consume(qb, sb);
-      if (bi + 3 < total) load_batch(qb, sb);
+      consume(qb);
+      if (bi + 3 < total) load_batch(qb);
     }
   }
-  // the next kernel may start on SMs this one leaves (it waits for our writes itself)
-  grid_dep_launch();
   if (CLUSTER) cg::this_cluster().sync();  // keep shared memory alive for remote readers
 }
 
@@ -389,30 +257,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
 // host side: plan + launch
 // ---------------------------------------------------------------------------
 // Chunks per load batch (double buffered): the chunk count of every K slice is
-// a multiple of it.  Q4 carries 12 registers per chunk and group, so it takes
-// two chunks per batch with one group per warp and one with two.
-__host__ __device__ constexpr int batch_chunks(int fmt, int G) {
-  return fmt == IL_BF16 ? 4 : (fmt == IL_Q8 ? 2 : (G == 1 ? 2 : 1));
-}
+// a multiple of it.
+constexpr int kBatchChunks = 4;
 
 using KernelFn = void (*)(DecodeParams);
 
-template <int FMT, int G, bool CLUSTER>
-KernelFn kernel_for() {
-  return decode_kernel<FMT, G, batch_chunks(FMT, G), CLUSTER>;
-}
-
-KernelFn select(int fmt, int G, bool cluster) {
-#define IL_SEL(F)                                                                      \
-  if (fmt == F) {                                                                      \
-    if (G == 1) return cluster ? kernel_for<F, 1, true>() : kernel_for<F, 1, false>(); \
-    return cluster ? kernel_for<F, 2, true>() : kernel_for<F, 2, false>();             \
-  }
-  IL_SEL(IL_BF16)
-  IL_SEL(IL_Q8)
-  IL_SEL(IL_Q4)
-#undef IL_SEL
-  return nullptr;
+KernelFn select(int G, bool cluster) {
+  if (G == 1) return cluster ? decode_kernel<1, kBatchChunks, true> : decode_kernel<1, kBatchChunks, false>;
+  return cluster ? decode_kernel<2, kBatchChunks, true> : decode_kernel<2, kBatchChunks, false>;
 }
 
 std::mutex g_occ_mu;
@@ -420,11 +272,16 @@ std::map<std::tuple<int, int, int, int, int, int>, int> g_occ;  // -> clusters (
 
 }  // namespace
 
-cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream, int num_sms,
-                          int* launches) {
+cudaError_t prepare_decode(int fmt, const DecodeParams& p, int num_sms, unsigned* status, void* ws,
+                           size_t ws_bytes, Launch* out) {
+  if (fmt == IL_BF16) return prepare_decode_bf16(p, num_sms, out);
+  return prepare_qdecode(fmt, p, num_sms, status, ws, ws_bytes, out);
+}
+
+cudaError_t prepare_decode_bf16(const DecodeParams& pin, int num_sms, Launch* out) {
   DecodeParams p = pin;
-  const int ck = chunk_k(fmt);
-  const int spc = ck / 16;
+  const int ck = kChunkK;
+  const int spc = kSlotsPerChunk;
   // Choose groups per warp G and the K split C (cluster size) so that the
   // (row block, K slice) tasks fill the resident CTA slots in whole rounds:
   // persistent clusters take row blocks round-robin, so a last round that is
@@ -435,7 +292,7 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
   int G = 1, C = -1, cps = 0;
   for (int g = 2; g >= 1; --g) {
     const int rowblocks = (p.total_groups + kWarps * g - 1) / (kWarps * g);
-    const int bc = batch_chunks(fmt, g);
+    const int bc = kBatchChunks;
     for (int c = c_min; c <= 8 && c <= p.n_chunks; ++c) {
       const int cp = ((p.n_chunks + c - 1) / c + bc - 1) / bc * bc;  // a multiple of the batch
       const int ce = (p.n_chunks + cp - 1) / cp;
@@ -456,7 +313,7 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
       }
     }
   }
-  if (C < 1 || C > 8 || p.n_chunks % batch_chunks(fmt, G) != 0) return cudaErrorInvalidValue;
+  if (C < 1 || C > 8 || p.n_chunks % kBatchChunks != 0) return cudaErrorInvalidValue;
   const int gpb = kWarps * G;
   p.n_rowblocks = (p.total_groups + gpb - 1) / gpb;
   p.slices = C;
@@ -464,14 +321,13 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
   const bool cluster = C > 1;
   const size_t smem = (size_t)cps * spc * 512 + (cluster ? 2 * gpb * 64 * sizeof(float) : 0);
 
-  KernelFn fn = select(fmt, G, cluster);
+  KernelFn fn = select(G, cluster);
   if (fn == nullptr) return cudaErrorInvalidValue;
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
   if (cluster) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = C;
@@ -486,7 +342,7 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
   int resident = 0;
   {
     std::lock_guard<std::mutex> lk(g_occ_mu);
-    auto key = std::make_tuple(dev, fmt, G, C, (int)cluster, (int)smem);
+    auto key = std::make_tuple(dev, 0, G, C, (int)cluster, (int)smem);
     auto it = g_occ.find(key);
     if (it != g_occ.end()) {
       resident = it->second;
@@ -517,19 +373,19 @@ cudaError_t launch_decode(int fmt, const DecodeParams& pin, cudaStream_t stream,
     }
   }
   const int nclusters = p.n_rowblocks < resident ? p.n_rowblocks : resident;
-  cfg.gridDim = dim3(nclusters * C);
+  Launch& L = *out;
+  L = Launch();
+  L.fn = reinterpret_cast<const void*>(fn);
+  L.grid = dim3(nclusters * C);
+  L.block = dim3(kThreads);
+  L.smem = smem;
+  if (cluster) L.set_cluster(C);
   // Early launch behind the previous kernel pays off when this grid fills every
   // resident slot; a smaller grid would be placed unevenly on the SMs that free
   // up first, so it waits for the previous kernel as usual.
-  if (kUsePdl && nclusters == resident) {
-    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs += 1;
-  }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p);
-  if (launches) ++*launches;
-  return e;
+  if (kUsePdl && nclusters == resident) L.allow_early_start();
+  if (!L.set_args(p)) return cudaErrorMemoryAllocation;
+  return cudaSuccess;
 }
 
 }  // namespace il

@@ -57,7 +57,9 @@ std::mutex g_dev_mu;
 std::map<int, DeviceState> g_devices;
 
 // Scratch of the tensor-core path, one set per (device, stream): the bf16 copy
-// of x and the split-K workspace.
+// of x and the split-K workspace.  Grown with the stream-ordered allocator, so
+// growing never waits for the stream: the old buffer is released in stream
+// order, after the work already queued that may still read it.
 struct Scratch {
   void* ptr = nullptr;
   size_t bytes = 0;
@@ -140,24 +142,47 @@ int64_t host_bytes(int format, int64_t n_out, int64_t n_in) {
   return n_out * (n_in / 2) + 4 * n_out * (n_in / 32);
 }
 
+cudaError_t il_malloc_async(void** p, size_t bytes, cudaStream_t stream) {
+  const char* env = getenv("IL_FAULT_ALLOC_FAIL_AFTER");
+  if (env != nullptr && *env != '\0') {
+    const long limit = strtol(env, nullptr, 10);
+    if (g_alloc_count.fetch_add(1) >= limit) {
+      *p = nullptr;
+      return cudaErrorMemoryAllocation;
+    }
+  }
+  return cudaMallocAsync(p, bytes, stream);
+}
+
+// Scratch may only grow outside stream capture: an allocation made while a
+// stream is captured would belong to the graph, not to the library.
+int check_not_capturing(cudaStream_t stream, const char* what) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cs != cudaStreamCaptureStatusNone)
+    return fail(IL_ERR_UNSUPPORTED,
+                "%s must grow while the stream is being captured: run one call of this size on the stream "
+                "before capturing it",
+                what);
+  return IL_OK;
+}
+
 int get_scratch(int dev, cudaStream_t stream, size_t bytes, void** out) {
   std::lock_guard<std::mutex> lk(g_scratch_mu);
   Scratch& s = g_scratch[{dev, stream}];
   if (s.bytes < bytes) {
-    if (s.ptr != nullptr) {
-      // The old buffer may still be read by work queued on `stream`.
-      cudaError_t e = cudaStreamSynchronize(stream);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-      cudaFree(s.ptr);
-      s.ptr = nullptr;
-      s.bytes = 0;
-    }
-    size_t want = bytes + bytes / 4;
-    cudaError_t e = il_malloc(&s.ptr, want);
+    const int rc = check_not_capturing(stream, "the bf16 copy of x");
+    if (rc != IL_OK) return rc;
+    const size_t want = bytes + bytes / 4;
+    void* np = nullptr;
+    cudaError_t e = il_malloc_async(&np, want, stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return fail(IL_ERR_OOM, "allocating %zu bytes of scratch failed", want);
     }
+    if (s.ptr != nullptr) cudaFreeAsync(s.ptr, stream);  // after the queued work that reads it
+    s.ptr = np;
     s.bytes = want;
   }
   *out = s.ptr;
@@ -168,22 +193,22 @@ int get_workspace(int dev, cudaStream_t stream, size_t bytes, void** out, size_t
   std::lock_guard<std::mutex> lk(g_scratch_mu);
   Scratch& s = g_scratch[{dev, stream}];
   if (s.ws_bytes < bytes) {
-    if (s.ws != nullptr) {
-      cudaError_t e = cudaStreamSynchronize(stream);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-      cudaFree(s.ws);
-      s.ws = nullptr;
-      s.ws_bytes = 0;
-    }
-    cudaError_t e = il_malloc(&s.ws, bytes);
+    const int rc = check_not_capturing(stream, "the split-K workspace");
+    if (rc != IL_OK) return rc;
+    void* np = nullptr;
+    cudaError_t e = il_malloc_async(&np, bytes, stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      s.ws = nullptr;
       return fail(IL_ERR_OOM, "allocating %zu bytes of split-K workspace failed", bytes);
     }
     // the per-tile arrival counters at its start must be zero before first use
-    e = cudaMemsetAsync(s.ws, 0, bytes, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace)");
+    e = cudaMemsetAsync(np, 0, bytes, stream);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(np, stream);
+      return cuda_fail(e, "cudaMemsetAsync(workspace)");
+    }
+    if (s.ws != nullptr) cudaFreeAsync(s.ws, stream);
+    s.ws = np;
     s.ws_bytes = bytes;
   }
   *out = s.ws;
@@ -205,23 +230,23 @@ int get_head_scratch(int dev, cudaStream_t stream, int64_t n_cent, int64_t k, ui
   std::lock_guard<std::mutex> lk(g_scratch_mu);
   HeadScratch& s = g_head_scratch[{dev, stream}];
   if (s.n_cent < n_cent || s.k < k) {
-    if (s.ptr != nullptr) {
-      cudaError_t e = cudaStreamSynchronize(stream);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-      cudaFree(s.ptr);
-      s.ptr = nullptr;
-      s.n_cent = s.k = 0;
-    }
+    const int rc = check_not_capturing(stream, "the LM-head scratch");
+    if (rc != IL_OK) return rc;
     const int64_t nc = std::max(n_cent, (int64_t)1024), kk = std::max(k, (int64_t)256);
     const size_t bytes = kHeadStateBytes + (size_t)nc * 4 + (size_t)kk * 4;
-    cudaError_t e = il_malloc(&s.ptr, bytes);
+    void* np = nullptr;
+    cudaError_t e = il_malloc_async(&np, bytes, stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      s.ptr = nullptr;
       return fail(IL_ERR_OOM, "allocating %zu bytes of LM-head scratch failed", bytes);
     }
-    e = cudaMemsetAsync(s.ptr, 0, bytes, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(LM-head scratch)");
+    e = cudaMemsetAsync(np, 0, bytes, stream);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(np, stream);
+      return cuda_fail(e, "cudaMemsetAsync(LM-head scratch)");
+    }
+    if (s.ptr != nullptr) cudaFreeAsync(s.ptr, stream);
+    s.ptr = np;
     s.n_cent = nc;
     s.k = kk;
   }
@@ -312,16 +337,14 @@ il_weight* upload_impl(const char* fn, int format, const void* const* host, int 
   w->glu = parts == 2 ? 1 : 0;
   w->n_out = rows;
   w->n_in = n_in;
-  w->n_out_pad = (rows + kGroupRows - 1) / kGroupRows * kGroupRows;
+  const int64_t pr = pad_rows(format);
+  w->n_out_pad = (rows + pr - 1) / pr * pr;
   w->n_in_pad = (n_in + kPadK - 1) / kPadK * kPadK;
   w->n_groups = w->n_out_pad / kGroupRows;
   w->n_chunks = w->n_in_pad / chunk_k(format);
   w->host_bytes = host_bytes(format, rows, n_in);
-  size_t qbytes = format == IL_BF16 ? (size_t)w->n_out_pad * w->n_in_pad * 2
-                                    : (size_t)w->n_groups * w->n_chunks * kChunkBytes;
-  size_t sbytes = format == IL_BF16 ? 0 : (size_t)w->n_groups * w->n_chunks * chunk_scale_bytes(format);
-  size_t soff = (qbytes + 255) / 256 * 256;
-  w->device_bytes = soff + sbytes;
+  w->device_bytes = format == IL_BF16 ? (size_t)w->n_out_pad * w->n_in_pad * 2
+                                      : (size_t)(w->n_out_pad / kPairRows) * w->n_chunks * record_bytes(format);
 
   void* mem = nullptr;
   cudaError_t e = il_malloc(&mem, w->device_bytes);
@@ -333,7 +356,6 @@ il_weight* upload_impl(const char* fn, int format, const void* const* host, int 
     return nullptr;
   }
   w->quants = static_cast<uint8_t*>(mem);
-  w->scales = sbytes ? reinterpret_cast<float*>(w->quants + soff) : nullptr;
 
   void* staging = nullptr;
   e = il_malloc(&staging, (size_t)w->host_bytes);
@@ -452,23 +474,58 @@ int il_check_device_status(void* stream) {
   const int dev = current_device(&ds);
   if (dev < 0) return dev;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  unsigned word = 0;
+  unsigned word = 0, noalloc_word = 0;
+  unsigned* noalloc = noalloc_status_word(dev);
   cudaError_t e = cudaMemcpyAsync(&word, ds->status, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && noalloc != nullptr)
+    e = cudaMemcpyAsync(&noalloc_word, noalloc, sizeof noalloc_word, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e == cudaSuccess) e = cudaMemsetAsync(ds->status, 0, sizeof word, s);
+  if (e == cudaSuccess && noalloc != nullptr) e = cudaMemsetAsync(noalloc, 0, sizeof noalloc_word, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "il_check_device_status");
+  word |= noalloc_word;
   if (word == kStatusBadToken) return fail(IL_ERR_ARG, "il_centroid_head met an ordering entry >= vocab");
   if (word != 0) {
     // a kernel that gave up may have left split-K arrival counters behind: clear
-    // this device's workspaces so the next launches start from zero
+    // this device's workspaces, once no stream still uses them, so the next
+    // launches start from zero
+    e = cudaDeviceSynchronize();
     {
       std::lock_guard<std::mutex> lk(g_scratch_mu);
       for (auto& kv : g_scratch)
-        if (kv.first.first == dev && kv.second.ws != nullptr) cudaMemset(kv.second.ws, 0, kv.second.ws_bytes);
+        if (kv.first.first == dev && kv.second.ws != nullptr && e == cudaSuccess)
+          e = cudaMemset(kv.second.ws, 0, kv.second.ws_bytes);
     }
+    size_t nb = 0;
+    void* nc = noalloc_split_counters(dev, &nb);
+    if (nc != nullptr && e == cudaSuccess) e = cudaMemset(nc, 0, nb);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "il_check_device_status: clearing the split-K workspaces");
     return fail(IL_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (code 0x%x)", word);
   }
+  return IL_OK;
+}
+
+int il_release_scratch(void* stream_) {
+  clear_error();
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  auto it = g_scratch.find({dev, stream});
+  if (it != g_scratch.end()) {
+    if (it->second.ptr != nullptr) e = cudaFreeAsync(it->second.ptr, stream);
+    if (e == cudaSuccess && it->second.ws != nullptr) e = cudaFreeAsync(it->second.ws, stream);
+    g_scratch.erase(it);
+  }
+  auto ih = g_head_scratch.find({dev, stream});
+  if (ih != g_head_scratch.end()) {
+    if (e == cudaSuccess && ih->second.ptr != nullptr) e = cudaFreeAsync(ih->second.ptr, stream);
+    g_head_scratch.erase(ih);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "il_release_scratch");
   return IL_OK;
 }
 
@@ -476,132 +533,41 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
                     void* stream_) {
   clear_error();
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (t < 0 || t > kMaxT) return fail(IL_ERR_ARG, "il_matmul_batch: t=%lld out of range", (long long)t);
-  if (n_jobs < 0 || n_jobs > kMaxJobs)
-    return fail(IL_ERR_ARG, "il_matmul_batch: n_jobs=%d out of range", n_jobs);
-  if (t == 0 || n_jobs == 0) return IL_OK;
-  if (x == nullptr) return fail(IL_ERR_ARG, "il_matmul_batch: x is NULL");
-  if (jobs == nullptr) return fail(IL_ERR_ARG, "il_matmul_batch: jobs is NULL");
-  if (reinterpret_cast<uintptr_t>(x) % 16 != 0)
-    return fail(IL_ERR_ARG, "il_matmul_batch: x is not 16-byte aligned");
-  if (n_in < 1 || n_in > kMaxNIn)
-    return fail(IL_ERR_SHAPE, "il_matmul_batch: n_in=%lld out of range", (long long)n_in);
-
+  int rc = check_batch_args(x, t, n_in, jobs, n_jobs);
+  if (rc != IL_OK || t == 0 || n_jobs == 0) return rc;
   DeviceState* ds = nullptr;
   const int dev = current_device(&ds);
   if (dev < 0) return dev;
-
-  // ---- validate every job before launching anything
-  std::vector<std::pair<uintptr_t, uintptr_t>> ranges;
-  ranges.reserve(n_jobs + 1);
-  ranges.emplace_back(reinterpret_cast<uintptr_t>(x),
-                      reinterpret_cast<uintptr_t>(x) + (uintptr_t)(t * n_in * 4));
+  std::vector<const PackedWeight*> ws;
   uint64_t wbytes = 0, flops = 0;
-  {
-    std::lock_guard<std::mutex> lk(g_reg_mu);
-    for (int j = 0; j < n_jobs; ++j) {
-      const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[j].w);
-      if (w == nullptr || g_registry.count(w) == 0 || w->magic != kWeightMagic)
-        return fail(IL_ERR_HANDLE, "il_matmul_batch: job %d has an invalid weight handle", j);
-      if (w->device != dev)
-        return fail(IL_ERR_HANDLE, "il_matmul_batch: job %d weight lives on device %d, current is %d",
-                    j, w->device, dev);
-      if (w->n_in != n_in)
-        return fail(IL_ERR_SHAPE, "il_matmul_batch: job %d weight n_in=%lld, batch n_in=%lld", j,
-                    (long long)w->n_in, (long long)n_in);
-      if (jobs[j].n_out != out_width(*w))
-        return fail(IL_ERR_SHAPE, "il_matmul_batch: job %d n_out=%lld, weight n_out=%lld", j,
-                    (long long)jobs[j].n_out, (long long)out_width(*w));
-      if (jobs[j].y == nullptr) return fail(IL_ERR_ARG, "il_matmul_batch: job %d y is NULL", j);
-      if (reinterpret_cast<uintptr_t>(jobs[j].y) % 4 != 0)
-        return fail(IL_ERR_ARG, "il_matmul_batch: job %d y is not 4-byte aligned", j);
-      const uintptr_t y0 = reinterpret_cast<uintptr_t>(jobs[j].y);
-      ranges.emplace_back(y0, y0 + (uintptr_t)(t * out_width(*w) * 4));
-      wbytes += (uint64_t)w->host_bytes;
-      flops += 2ull * (uint64_t)t * (uint64_t)n_in * (uint64_t)w->n_out;
-    }
-  }
-  std::vector<std::pair<uintptr_t, uintptr_t>> sorted = ranges;
-  std::sort(sorted.begin(), sorted.end());
-  for (size_t i = 1; i < sorted.size(); ++i)
-    if (overlaps(sorted[i - 1].first, sorted[i - 1].second, sorted[i].first, sorted[i].second))
-      return fail(IL_ERR_ARG, "il_matmul_batch: x and the y buffers must not overlap");
+  rc = api_check_batch(x, t, n_in, jobs, n_jobs, dev, &ws, &wbytes, &flops);
+  if (rc != IL_OK) return rc;
 
-  // ---- dispatch: large t -> cast x once + one tensor-core GEMM launch per format
-  // (Q8/Q4 weights are dequantised in shared memory inside it); everything else
-  // -> decode kernel (token groups of 8), one launch per format present.
-  int launches = 0;
-  cudaError_t e = cudaSuccess;
-  const bool gemm_bf16 = t >= kGemmMinT;
-  const bool gemm_quant = t >= kGemmMinTQuant;
-  if (gemm_bf16) {
-    std::vector<GemmJob> gj[3];
-    int64_t n_in_pad = 0;
-    for (int j = 0; j < n_jobs; ++j) {
-      const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[j].w);
-      n_in_pad = w->n_in_pad;
-      if (w->format == IL_BF16 || gemm_quant) gj[w->format].push_back(GemmJob{w, jobs[j].y});
-    }
-    if (!gj[0].empty() || !gj[1].empty() || !gj[2].empty()) {
-      void* xb = nullptr;
-      const int rc = get_scratch(dev, stream, (size_t)t * (size_t)n_in_pad * 2, &xb);
-      if (rc != IL_OK) return rc;
-      void* ws = nullptr;
-      size_t ws_bytes = 0;
-      for (int f = 0; f < 3; ++f)
-        if (!gj[f].empty())
-          ws_bytes = std::max(ws_bytes, gemm_workspace_bytes(t, n_in_pad, gj[f].data(), (int)gj[f].size(),
-                                                             ds->num_sms));
-      if (ws_bytes > 0) {
-        const int rc2 = get_workspace(dev, stream, ws_bytes, &ws, &ws_bytes);
-        if (rc2 != IL_OK) return rc2;
-      }
-      e = launch_cast_bf16(x, t, n_in, n_in_pad, static_cast<__nv_bfloat16*>(xb), stream);
-      if (e == cudaSuccess) ++launches;
-      for (int f = 0; f < 3 && e == cudaSuccess; ++f)
-        if (!gj[f].empty())
-          e = launch_gemm(f, static_cast<const __nv_bfloat16*>(xb), t, n_in_pad, gj[f].data(), (int)gj[f].size(),
-                          stream, ds->num_sms, ds->status, &launches, ws, ws_bytes);
-    }
+  // ---- plan, scratch, and every launch prepared before the first is enqueued
+  BatchPlan plan;
+  plan_batch(t, jobs, n_jobs, ws, /*gemm_quant=*/true, &plan);
+  void* xb = nullptr;
+  void* wsp = nullptr;
+  size_t ws_bytes = 0;
+  if (plan.xb_bytes > 0) {
+    rc = get_scratch(dev, stream, plan.xb_bytes, &xb);
+    if (rc != IL_OK) return rc;
   }
-  for (int fmt = IL_BF16; fmt <= IL_Q4 && e == cudaSuccess; ++fmt) {
-    if (fmt == IL_BF16 ? gemm_bf16 : gemm_quant) continue;
-    std::vector<int> idx;
-    for (int j = 0; j < n_jobs; ++j)
-      if (reinterpret_cast<const PackedWeight*>(jobs[j].w)->format == fmt) idx.push_back(j);
-    if (idx.empty()) continue;
-    for (size_t j0 = 0; j0 < idx.size() && e == cudaSuccess; j0 += kMaxDecodeJobs) {
-      const size_t j1 = std::min(idx.size(), j0 + (size_t)kMaxDecodeJobs);
-      for (int64_t t0 = 0; t0 < t && e == cudaSuccess; t0 += 8) {
-        DecodeParams p;
-        memset(&p, 0, sizeof p);
-        p.x = x + t0 * n_in;
-        p.t = (int)std::min<int64_t>(8, t - t0);
-        p.x_row_stride = (int)n_in;
-        p.n_in = (int)n_in;
-        int groups = 0;
-        for (size_t j = j0; j < j1; ++j) {
-          const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[idx[j]].w);
-          DecodeJob& dj = p.jobs[p.n_jobs++];
-          dj.w = w->quants;
-          dj.s = w->scales;
-          dj.y = jobs[idx[j]].y + t0 * out_width(*w);
-          dj.n_out = (int32_t)w->n_out;
-          dj.glu = w->glu;
-          dj.group_begin = groups;
-          dj.row_stride = fmt == IL_BF16 ? w->n_in_pad : w->n_chunks;
-          groups += (int)w->n_groups;
-          p.n_chunks = (int)w->n_chunks;
-        }
-        p.total_groups = groups;
-        e = launch_decode(fmt, p, stream, ds->num_sms, &launches);
-      }
-    }
+  const size_t want = plan_workspace_bytes(plan, t, n_in, jobs, ws, ds->num_sms);
+  if (want > 0) {
+    rc = get_workspace(dev, stream, want, &wsp, &ws_bytes);
+    if (rc != IL_OK) return rc;
   }
+  std::vector<Launch> launches;
+  cudaError_t e = prepare_batch(plan, x, t, n_in, jobs, ws, static_cast<__nv_bfloat16*>(xb), wsp, ws_bytes,
+                                ds->num_sms, ds->status, &launches);
+  if (e != cudaSuccess) return cuda_fail(e, "il_matmul_batch: preparing the launches");
+  int n_launched = 0;
+  e = run_launches(launches, stream, &n_launched);
+  g_stats.launches.fetch_add((uint64_t)n_launched);
   if (e != cudaSuccess) return cuda_fail(e, "il_matmul_batch: launch");
   g_stats.batches.fetch_add(1);
   g_stats.jobs.fetch_add((uint64_t)n_jobs);
-  g_stats.launches.fetch_add((uint64_t)launches);
   g_stats.weight_bytes.fetch_add(wbytes);
   g_stats.flops.fetch_add(flops);
   return IL_OK;
@@ -646,28 +612,157 @@ int il_centroid_head(const float* x, int64_t h, const il_weight* centroids_h, co
   if (rc != IL_OK) return rc;
   float* cl = reinterpret_cast<float*>(scratch + kHeadStateBytes);
   uint32_t* sel = selected_out != nullptr ? selected_out : reinterpret_cast<uint32_t*>(cl + std::max(n_cent, (int64_t)1024));
-  // 1. centroid logits: a one-job batch on the decode kernel
+  // 1. centroid logits: a one-job batch on the decode kernel; 2-3. selection,
+  // cluster logits and first maximum -- all prepared before any is enqueued
   il_job job{centroids_h, n_cent, cl};
-  rc = il_matmul_batch(x, 1, h, &job, 1, stream_);
-  if (rc != IL_OK) return rc;
-  // 2-4. selection, cluster logits, first maximum
-  int launches = 0;
-  cudaError_t e = launch_lmhead(x, (int)h, cl, (int)n_cent, (int)k, *ew, ordering, (int)per, sel, scores_out,
-                                reinterpret_cast<unsigned long long*>(scratch),
-                                reinterpret_cast<unsigned*>(scratch + 8), token_out, score_out, ds->status, stream,
-                                ds->num_sms, &launches);
-  g_stats.launches.fetch_add((uint64_t)launches);
+  std::vector<const PackedWeight*> ws{cw};
+  BatchPlan plan;
+  plan_batch(1, &job, 1, ws, true, &plan);
+  std::vector<Launch> launches;
+  cudaError_t e = prepare_batch(plan, x, 1, h, &job, ws, nullptr, nullptr, 0, ds->num_sms, ds->status, &launches);
+  if (e == cudaSuccess)
+    e = prepare_lmhead(x, (int)h, cl, (int)n_cent, (int)k, *ew, ordering, (int)per, sel, scores_out,
+                       reinterpret_cast<unsigned long long*>(scratch), reinterpret_cast<unsigned*>(scratch + 8),
+                       token_out, score_out, ds->status, ds->num_sms, &launches);
+  if (e != cudaSuccess) return cuda_fail(e, "il_centroid_head: preparing the launches");
+  int n_launched = 0;
+  e = run_launches(launches, stream, &n_launched);
+  g_stats.launches.fetch_add((uint64_t)n_launched);
   if (e != cudaSuccess) return cuda_fail(e, "il_centroid_head: launch");
+  g_stats.batches.fetch_add(1);
+  g_stats.jobs.fetch_add(1);
+  g_stats.weight_bytes.fetch_add((uint64_t)cw->host_bytes);
+  g_stats.flops.fetch_add(2ull * (uint64_t)h * (uint64_t)n_cent);
   return IL_OK;
 }
 
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
-// Helpers for entry points defined in other translation units (they read the
-// handle registry, the error state and the counters kept here).
+// Batch planning shared by il_matmul_batch, il_matmul_batch_noalloc and the
+// centroid head, and helpers for entry points defined in other translation
+// units (they read the handle registry, the error state and the counters kept
+// here).
 // ---------------------------------------------------------------------------
 namespace il {
+
+cudaError_t run_launches(const std::vector<Launch>& v, cudaStream_t stream, int* launches) {
+  for (const Launch& L : v) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = L.grid;
+    cfg.blockDim = L.block;
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = stream;
+    cfg.attrs = const_cast<cudaLaunchAttribute*>(L.attr);
+    cfg.numAttrs = L.nattr;
+    cudaError_t e = cudaLaunchKernelExC(&cfg, L.fn, const_cast<void**>(L.args));
+    if (launches) ++*launches;
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+void plan_batch(int64_t t, const il_job* jobs, int n_jobs, const std::vector<const PackedWeight*>& ws,
+                bool gemm_quant, BatchPlan* plan) {
+  *plan = BatchPlan();
+  const bool gemm_bf16 = t >= kGemmMinT;
+  const bool gemm_q = gemm_quant && t >= kGemmMinTQuant;
+  for (int j = 0; j < n_jobs; ++j) {
+    const PackedWeight* w = ws[j];
+    const bool gemm = w->format == IL_BF16 ? gemm_bf16 : gemm_q;
+    if (gemm) {
+      plan->gemm[w->format].push_back(GemmJob{w, jobs[j].y});
+      plan->n_in_pad = w->n_in_pad;
+    } else {
+      plan->decode[w->format].push_back(j);
+    }
+  }
+  if (!plan->gemm[0].empty() || !plan->gemm[1].empty() || !plan->gemm[2].empty())
+    plan->xb_bytes = (size_t)t * (size_t)plan->n_in_pad * 2;
+}
+
+namespace {
+
+// The decode launches of a plan, in launch order: one per format, per
+// kMaxDecodeJobs jobs and per 8 tokens.
+void decode_launch_params(const BatchPlan& plan, const float* x, int64_t t, int64_t n_in, const il_job* jobs,
+                          const std::vector<const PackedWeight*>& ws, std::vector<std::pair<int, DecodeParams>>* out) {
+  for (int fmt = IL_BF16; fmt <= IL_Q4; ++fmt) {
+    const std::vector<int>& idx = plan.decode[fmt];
+    for (size_t j0 = 0; j0 < idx.size(); j0 += kMaxDecodeJobs) {
+      const size_t j1 = std::min(idx.size(), j0 + (size_t)kMaxDecodeJobs);
+      for (int64_t t0 = 0; t0 < t; t0 += 8) {
+        DecodeParams p;
+        memset(&p, 0, sizeof p);
+        p.x = x != nullptr ? x + t0 * n_in : nullptr;
+        p.t = (int)std::min<int64_t>(8, t - t0);
+        p.x_row_stride = (int)n_in;
+        p.n_in = (int)n_in;
+        int groups = 0;
+        for (size_t j = j0; j < j1; ++j) {
+          const PackedWeight* w = ws[idx[j]];
+          DecodeJob& dj = p.jobs[p.n_jobs++];
+          dj.w = w->quants;
+          dj.y = jobs[idx[j]].y + t0 * out_width(*w);
+          dj.n_out = (int32_t)w->n_out;
+          dj.glu = w->glu;
+          dj.group_begin = groups;
+          dj.row_stride = fmt == IL_BF16 ? w->n_in_pad : w->n_chunks;
+          groups += (int)w->n_groups;
+          p.n_chunks = (int)w->n_chunks;
+        }
+        p.total_groups = groups;
+        out->emplace_back(fmt, p);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+size_t plan_workspace_bytes(const BatchPlan& plan, int64_t t, int64_t n_in, const il_job* jobs,
+                            const std::vector<const PackedWeight*>& ws, int num_sms) {
+  size_t need = 0;
+  for (int f = 0; f < 3; ++f)
+    if (!plan.gemm[f].empty())
+      need = std::max(need, gemm_workspace_bytes(t, plan.n_in_pad, plan.gemm[f].data(), (int)plan.gemm[f].size(),
+                                                 num_sms));
+  std::vector<std::pair<int, DecodeParams>> dl;
+  decode_launch_params(plan, nullptr, t, n_in, jobs, ws, &dl);
+  for (const auto& fp : dl)
+    if (fp.first != IL_BF16) need = std::max(need, qdecode_workspace_bytes(fp.first, fp.second, num_sms));
+  return need;
+}
+
+cudaError_t prepare_batch(const BatchPlan& plan, const float* x, int64_t t, int64_t n_in, const il_job* jobs,
+                          const std::vector<const PackedWeight*>& ws, __nv_bfloat16* xb, void* wsp,
+                          size_t ws_bytes, int num_sms, unsigned* status, std::vector<Launch>* out) {
+  // large t: x cast to bf16 once, then one tensor-core launch per format (and
+  // per kMaxGemmJobs jobs)
+  if (plan.xb_bytes > 0) {
+    if (xb == nullptr) return cudaErrorInvalidValue;
+    Launch cast;
+    cudaError_t e = prepare_cast_bf16(x, t, n_in, plan.n_in_pad, xb, &cast);
+    if (e != cudaSuccess) return e;
+    out->push_back(cast);
+    for (int f = 0; f < 3; ++f)
+      if (!plan.gemm[f].empty()) {
+        e = prepare_gemm(f, xb, t, plan.n_in_pad, plan.gemm[f].data(), (int)plan.gemm[f].size(), num_sms, status,
+                         wsp, ws_bytes, out);
+        if (e != cudaSuccess) return e;
+      }
+  }
+  // small t: the decode kernel
+  std::vector<std::pair<int, DecodeParams>> dl;
+  decode_launch_params(plan, x, t, n_in, jobs, ws, &dl);
+  for (const auto& fp : dl) {
+    Launch L;
+    cudaError_t e = prepare_decode(fp.first, fp.second, num_sms, status, wsp, ws_bytes, &L);
+    if (e != cudaSuccess) return e;
+    out->push_back(L);
+  }
+  return cudaSuccess;
+}
 
 void api_clear_error() { clear_error(); }
 
@@ -675,21 +770,29 @@ int api_fail(int code, const char* msg) { return fail(code, "%s", msg); }
 
 int api_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 
-// The same checks il_matmul_batch makes, on the calling thread's device `dev`;
-// on success fills `ws` with the weight of each job.
-int api_check_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs, int dev,
-                    std::vector<const PackedWeight*>* ws, uint64_t* wbytes, uint64_t* flops) {
+// The checks that need no device: sizes, null pointers, x alignment.
+int check_batch_args(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs) {
   if (t < 0 || t > kMaxT) return fail(IL_ERR_ARG, "t=%lld out of range", (long long)t);
   if (n_jobs < 0 || n_jobs > kMaxJobs) return fail(IL_ERR_ARG, "n_jobs=%d out of range", n_jobs);
-  ws->clear();
-  *wbytes = 0;
-  *flops = 0;
   if (t == 0 || n_jobs == 0) return IL_OK;
   if (x == nullptr) return fail(IL_ERR_ARG, "x is NULL");
   if (jobs == nullptr) return fail(IL_ERR_ARG, "jobs is NULL");
   if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return fail(IL_ERR_ARG, "x is not 16-byte aligned");
   if (n_in < 1 || n_in > kMaxNIn) return fail(IL_ERR_SHAPE, "n_in=%lld out of range", (long long)n_in);
+  return IL_OK;
+}
+
+// Every job's checks on the calling thread's device `dev`; on success fills `ws`
+// with the weight of each job.
+int api_check_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs, int dev,
+                    std::vector<const PackedWeight*>* ws, uint64_t* wbytes, uint64_t* flops) {
+  ws->clear();
+  *wbytes = 0;
+  *flops = 0;
+  int rc = check_batch_args(x, t, n_in, jobs, n_jobs);
+  if (rc != IL_OK || t == 0 || n_jobs == 0) return rc;
   std::vector<std::pair<uintptr_t, uintptr_t>> ranges;
+  ranges.reserve(n_jobs + 1);
   ranges.emplace_back(reinterpret_cast<uintptr_t>(x), reinterpret_cast<uintptr_t>(x) + (uintptr_t)(t * n_in * 4));
   {
     std::lock_guard<std::mutex> lk(g_reg_mu);
@@ -697,7 +800,8 @@ int api_check_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
       const PackedWeight* w = reinterpret_cast<const PackedWeight*>(jobs[j].w);
       if (w == nullptr || g_registry.count(w) == 0 || w->magic != kWeightMagic)
         return fail(IL_ERR_HANDLE, "job %d has an invalid weight handle", j);
-      if (w->device != dev) return fail(IL_ERR_HANDLE, "job %d weight lives on device %d", j, w->device);
+      if (w->device != dev)
+        return fail(IL_ERR_HANDLE, "job %d weight lives on device %d, current is %d", j, w->device, dev);
       if (w->n_in != n_in) return fail(IL_ERR_SHAPE, "job %d weight n_in=%lld, batch n_in=%lld", j,
                                        (long long)w->n_in, (long long)n_in);
       if (jobs[j].n_out != out_width(*w)) return fail(IL_ERR_SHAPE, "job %d n_out=%lld, weight n_out=%lld", j,

@@ -9,6 +9,11 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <cstdlib>
+#include <cstring>
+#include <memory>
+#include <vector>
+
 #include "../../include/il.h"
 
 namespace il {
@@ -16,20 +21,26 @@ namespace il {
 // ---------------------------------------------------------------------------
 // Packed device layout
 // ---------------------------------------------------------------------------
-// Rows are padded to a multiple of 8 (one "row group", the n=8 side of the
-// decode MMA) and columns to a multiple of 256 (two Q4 chunks, so every
-// format's chunk count is even); padding is 0.
-//
-// BF16: plain row-major u16 [n_out_pad][n_in_pad].  The decode kernel reads
-//   16 bytes (8 consecutive k) per lane; the tensor-core kernel tiles it with
-//   TMA (K-major, 128-byte swizzle).
-// Q8 / Q4: chunk-major.  A chunk is 8 rows x kChunkK columns and is exactly
-//   512 bytes of quants: lane L of a warp owns bytes [16L, 16L+16) of it.
-//   With n = L/4 (row in group) and q = L%4, the 16 bytes hold the elements
-//   the lane feeds to the MMAs of that chunk (see pack.cu for the order).
-//   Scales are a separate chunk-major stream: for each (group, chunk) and each
-//   q = 0..3, the scales of rows 2q and 2q+1 for every 32-block of the chunk.
+// BF16: plain row-major u16 [n_out_pad][n_in_pad], rows padded to a multiple of
+//   8 and columns to a multiple of 256 (zeros).  The decode kernel reads 16 bytes
+//   (8 consecutive k) per lane; the tensor-core kernel tiles it with TMA
+//   (K-major, 128-byte swizzle).
+// Q8 / Q4: rows padded to a multiple of 16 (a "pair" of two 8-row groups),
+//   columns to a multiple of 256; the weight is a sequence of records, one per
+//   (pair, chunk), pair-major: record (p, c) at byte (p * n_chunks + c) * RS.
+//   A chunk is kChunkK columns (Q8: 64, Q4: 128), so a group's quants in one
+//   chunk are exactly 512 bytes.  A record holds
+//     [0, 512)          quants of group 2p   (rows 16p .. 16p+7)
+//     [512, 1024)       quants of group 2p+1 (rows 16p+8 .. 16p+15)
+//     [1024, 1024+SB)   fp32 scales of group 2p, [8 rows][blocks of the chunk]
+//     [1024+SB, RS)     fp32 scales of group 2p+1
+//   with SB = 32 * blocks_per_chunk.  In a group's 512 bytes, lane L = 4n + q of
+//   a warp owns bytes [16L, 16L+16): the elements of row n that the lane feeds to
+//   the MMAs of that chunk (see pack.cu for the order).  Q8 bytes are stored
+//   biased, u = q + 128, so that one byte permute makes fp16 1024 + u.
+//   Padding decodes to q = 0 with scale 0.
 constexpr int kGroupRows = 8;
+constexpr int kPairRows = 16;
 constexpr int kPadK = 256;
 constexpr int kChunkBytes = 512;
 
@@ -37,6 +48,10 @@ __host__ __device__ constexpr int chunk_k(int fmt) { return fmt == IL_BF16 ? 32 
 __host__ __device__ constexpr int blocks_per_chunk(int fmt) { return fmt == IL_Q8 ? 2 : (fmt == IL_Q4 ? 4 : 0); }
 // Scale bytes per (group, chunk): 8 rows x blocks x 4 bytes.
 __host__ __device__ constexpr int chunk_scale_bytes(int fmt) { return 32 * blocks_per_chunk(fmt); }
+// Bytes of one (pair, chunk) record of a Q8 / Q4 weight: 1152 (Q8), 1280 (Q4).
+__host__ __device__ constexpr int record_bytes(int fmt) { return 2 * kChunkBytes + 2 * chunk_scale_bytes(fmt); }
+// Row padding of the packed layout.
+__host__ __device__ constexpr int pad_rows(int fmt) { return fmt == IL_BF16 ? kGroupRows : kPairRows; }
 
 // A gate+up weight (il_upload_gate_up) is stored as one matrix of n_out = 2*width
 // rows, row 2r = gate row r and row 2r+1 = up row r; its jobs write
@@ -49,8 +64,7 @@ struct PackedWeight {
   int64_t n_out, n_in;         // n_out: packed rows (2 * width of h for glu)
   int64_t n_out_pad, n_in_pad;
   int64_t n_groups, n_chunks;  // n_out_pad / 8, n_in_pad / chunk_k
-  uint8_t* quants;             // device, packed as above
-  float* scales;               // device, Q8/Q4 only
+  uint8_t* quants;             // device, packed as above (Q8/Q4: the records, scales inside)
   int64_t host_bytes;          // WeightRef::bytes
   size_t device_bytes;
 };
@@ -65,12 +79,11 @@ inline int64_t out_width(const PackedWeight& w) { return w.glu ? w.n_out / 2 : w
 constexpr int kMaxDecodeJobs = 32;
 
 struct DecodeJob {
-  const uint8_t* w;      // packed quants / bf16
-  const float* s;        // packed scales (Q8/Q4)
+  const uint8_t* w;      // packed weight (bf16 rows, or Q8/Q4 records)
   float* y;              // [t][n_out], or h [t][n_out / 2] when glu
   int32_t n_out;         // packed rows
-  int32_t group_begin;   // first global group index of this job
-  int64_t row_stride;    // bf16: n_in_pad (elements); Q: n_chunks (chunks per group)
+  int32_t group_begin;   // first global 8-row group of this job (even for Q8/Q4)
+  int64_t row_stride;    // bf16: n_in_pad (elements); Q8/Q4: n_chunks
   int32_t glu;           // rows interleaved gate/up: store gelu(g) * u
   int32_t pad_;
 };
@@ -108,9 +121,9 @@ __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol
 // fp16 decoders (the Q8/Q4 matmul path multiplies fp16 weights by fp16 x):
 // every |q| <= 128 is exact in fp16, and the fp16 with biased exponent 25 is
 // 1024 + its 10-bit mantissa, so one byte permute builds 1024 + u from a byte u.
-// Q8: word of 4 int8 -> fp16x2 pairs (e0,e1), (e2,e3), each exactly q.
-__device__ __forceinline__ void q8_word_to_f16x2(uint32_t word, uint32_t& p01, uint32_t& p23) {
-  const uint32_t u = word ^ 0x80808080u;                   // q + 128 as unsigned bytes
+// Q8: word of 4 packed bytes u = q + 128 -> fp16x2 pairs (e0,e1), (e2,e3), each
+// exactly q.
+__device__ __forceinline__ void q8_word_to_f16x2(uint32_t u, uint32_t& p01, uint32_t& p23) {
   uint32_t a = __byte_perm(u, 0x64646464u, 0x5140);        // [u0, 0x64, u1, 0x64]
   uint32_t b = __byte_perm(u, 0x64646464u, 0x5342);        // [u2, 0x64, u3, 0x64]
   const __half2 bias = __floats2half2_rn(1152.0f, 1152.0f);  // 1024 + 128
@@ -165,19 +178,98 @@ __device__ __forceinline__ float gelu_mul(float g, float u) {
 }
 
 // ---------------------------------------------------------------------------
-// Launchers (each returns a cudaError_t; the API layer maps it to il_status)
+// Prepared launches
 // ---------------------------------------------------------------------------
+// A kernel launch worked out in full on the host -- grid, attributes, and the
+// argument values copied into storage the record owns.  Every entry point
+// prepares all launches of a call (plans, tensor maps, occupancy queries, size
+// checks) before it enqueues the first, so a call that fails while preparing
+// has enqueued nothing.
+struct Launch {
+  const void* fn = nullptr;
+  dim3 grid, block;
+  size_t smem = 0;
+  cudaLaunchAttribute attr[3];
+  int nattr = 0;
+  std::shared_ptr<unsigned char> store;
+  void* args[16];
+  int nargs = 0;
+
+  // Copies the arguments (each of the kernel's parameter type) into 64-byte
+  // aligned storage.  False if the host allocation fails.
+  template <class... A>
+  bool set_args(const A&... a) {
+    constexpr size_t n = sizeof...(A);
+    static_assert(n >= 1 && n <= 16, "1 to 16 kernel arguments");
+    const size_t sizes[n] = {sizeof(A)...};
+    const size_t aligns[n] = {alignof(A)...};
+    const void* srcs[n] = {static_cast<const void*>(&a)...};
+    size_t offs[n];
+    size_t total = 0;
+    for (size_t i = 0; i < n; ++i) {
+      const size_t al = aligns[i] > 16 ? aligns[i] : 16;
+      total = (total + al - 1) / al * al;
+      offs[i] = total;
+      total += sizes[i];
+    }
+    unsigned char* mem = static_cast<unsigned char*>(std::aligned_alloc(64, (total + 63) / 64 * 64));
+    if (mem == nullptr) return false;
+    store.reset(mem, std::free);
+    for (size_t i = 0; i < n; ++i) {
+      std::memcpy(mem + offs[i], srcs[i], sizes[i]);
+      args[i] = mem + offs[i];
+    }
+    nargs = (int)n;
+    return true;
+  }
+  void allow_early_start() {  // programmatic dependent launch (see grid_dep_wait)
+    attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+    ++nattr;
+  }
+  void set_cluster(int c) {
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = c;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
+  }
+};
+
+// Enqueues the prepared launches in order on `stream`, counting each in
+// *launches.  Stops at the first launch the runtime rejects.
+cudaError_t run_launches(const std::vector<Launch>& v, cudaStream_t stream, int* launches);
+
+// Upload-time repack and the dequantise hook: single launches, enqueued directly.
 cudaError_t launch_pack(const PackedWeight& w, const uint8_t* staging, cudaStream_t stream);
 cudaError_t launch_dequant(const PackedWeight& w, float* out, cudaStream_t stream);
-cudaError_t launch_decode(int fmt, const DecodeParams& p, cudaStream_t stream, int num_sms,
-                          int* launches);
-cudaError_t launch_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_in_pad,
-                             __nv_bfloat16* out, cudaStream_t stream);
+// Decode kernel for t <= 8 tokens: bf16 weights run the register-streaming kernel
+// (gemv.cu), Q8 / Q4 weights the shared-memory ring kernel (qdecode.cu), whose
+// bounded waits record a code in `status` when they give up.
+cudaError_t prepare_decode(int fmt, const DecodeParams& p, int num_sms, unsigned* status, void* ws,
+                           size_t ws_bytes, Launch* out);
+cudaError_t prepare_decode_bf16(const DecodeParams& p, int num_sms, Launch* out);
+// ws / ws_bytes: split workspace (nullptr: K is never split over CTAs).
+cudaError_t prepare_qdecode(int fmt, const DecodeParams& p, int num_sms, unsigned* status, void* ws,
+                            size_t ws_bytes, Launch* out);
+// Split workspace the Q8/Q4 decode launch of `p` would use given unlimited room
+// (0: none).
+size_t qdecode_workspace_bytes(int fmt, const DecodeParams& p, int num_sms);
+cudaError_t prepare_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_in_pad, __nv_bfloat16* out,
+                              Launch* L);
 
 // Token counts from which a batch takes the tensor-core path instead of the
 // decode kernel (which streams the weights once per 8 tokens).
 constexpr int64_t kGemmMinT = 9;        // bf16 weights
 constexpr int64_t kGemmMinTQuant = 17;  // Q8 / Q4 weights
+
+// Split workspace (split-K of the tensor-core kernel, K split over CTAs of the
+// Q8/Q4 decode kernel): a fixed block of per-tile arrival counters, then the
+// partial results.  The counters read zero before every launch: the last
+// arriver of each tile puts its counter back, and a new workspace starts
+// zeroed; a launch with more tiles than counters does not split.
+constexpr int kSplitCounters = 65536;
+constexpr size_t kSplitCounterBytes = (size_t)kSplitCounters * sizeof(unsigned);
 
 struct GemmJob {
   const PackedWeight* w;
@@ -189,10 +281,45 @@ struct GemmJob {
 // ws / ws_bytes: split-K workspace (counters, then fp32 partial tiles); with
 // nullptr the kernel never splits K.  gemm_workspace_bytes gives the size the
 // launch plan wants (0 when no launch splits K).
-cudaError_t launch_gemm(int fmt, const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs,
-                        int n_jobs, cudaStream_t stream, int num_sms, unsigned* status, int* launches, void* ws,
-                        size_t ws_bytes);
+// Appends one launch per group of at most kMaxGemmJobs jobs to *out.
+cudaError_t prepare_gemm(int fmt, const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs,
+                         int n_jobs, int num_sms, unsigned* status, void* ws, size_t ws_bytes,
+                         std::vector<Launch>* out);
 size_t gemm_workspace_bytes(int64_t t, int64_t n_in_pad, const GemmJob* jobs, int n_jobs, int num_sms);
+
+// How a batch splits over the kernels: tensor-core jobs per format (large t)
+// and decode jobs per format (indices into the caller's jobs).
+struct BatchPlan {
+  std::vector<GemmJob> gemm[3];
+  std::vector<int> decode[3];
+  int64_t n_in_pad = 0;
+  size_t xb_bytes = 0;  // the bf16 copy of x the tensor-core jobs read (0: none)
+};
+// gemm_quant: Q8/Q4 jobs take the tensor-core path from kGemmMinTQuant tokens.
+void plan_batch(int64_t t, const il_job* jobs, int n_jobs, const std::vector<const PackedWeight*>& ws,
+                bool gemm_quant, BatchPlan* plan);
+// Split workspace the plan's launches would use (0: none).
+size_t plan_workspace_bytes(const BatchPlan& plan, int64_t t, int64_t n_in, const il_job* jobs,
+                            const std::vector<const PackedWeight*>& ws, int num_sms);
+// Appends every launch of the batch to *out (nothing is enqueued).  xb: the bf16
+// copy of x (plan.xb_bytes); wsp / ws_bytes: split-K workspace or nullptr / 0.
+cudaError_t prepare_batch(const BatchPlan& plan, const float* x, int64_t t, int64_t n_in, const il_job* jobs,
+                          const std::vector<const PackedWeight*>& ws, __nv_bfloat16* xb, void* wsp,
+                          size_t ws_bytes, int num_sms, unsigned* status, std::vector<Launch>* out);
+
+// Argument checks shared by the batch entry points (set the thread's error on failure).
+int check_batch_args(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs);
+int api_check_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs, int dev,
+                    std::vector<const PackedWeight*>* ws, uint64_t* wbytes, uint64_t* flops);
+void api_clear_error();
+int api_fail(int code, const char* msg);
+int api_cuda_fail(cudaError_t e, const char* what);
+void api_count_batch(int n_jobs, int launches, uint64_t wbytes, uint64_t flops);
+// Device address of il_matmul_batch_noalloc's status word on device `dev`, or
+// nullptr before that entry point has set the device up.
+unsigned* noalloc_status_word(int dev);
+// Its split workspace's arrival counters (nullptr before set-up).
+void* noalloc_split_counters(int dev, size_t* bytes);
 
 // Centroid-masked LM head after the centroid logits cl [n_cent] are computed:
 // top-k selection (sel [k]), the gathered cluster logits (scores_out [k*per],
@@ -201,9 +328,9 @@ size_t gemm_workspace_bytes(int64_t t, int64_t n_in_pad, const GemmJob* jobs, in
 constexpr int kMaxCentroids = 16384;   // the selection sorts them in one CTA's shared memory
 constexpr unsigned kStatusBadToken = 0x100;  // status word: an ordering entry >= vocab was skipped
 constexpr int kMaxHeadWidth = 32768;   // x is staged in shared memory as fp32
-cudaError_t launch_lmhead(const float* x, int h, const float* cl, int n_cent, int k, const PackedWeight& embed,
-                          const uint32_t* ordering, int per, uint32_t* sel, float* scores_out,
-                          unsigned long long* best_key, unsigned* done, uint32_t* token_out, float* score_out,
-                          unsigned* status, cudaStream_t stream, int num_sms, int* launches);
+cudaError_t prepare_lmhead(const float* x, int h, const float* cl, int n_cent, int k, const PackedWeight& embed,
+                           const uint32_t* ordering, int per, uint32_t* sel, float* scores_out,
+                           unsigned long long* best_key, unsigned* done, uint32_t* token_out, float* score_out,
+                           unsigned* status, int num_sms, std::vector<Launch>* out);
 
 }  // namespace il

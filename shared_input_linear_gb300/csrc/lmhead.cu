@@ -260,10 +260,10 @@ size_t topk_smem(int n_cent, int k) {
                         : ((size_t)n_cent + (size_t)pk) * sizeof(unsigned long long);
 }
 
-cudaError_t launch_lmhead(const float* x, int h, const float* cl, int n_cent, int k, const PackedWeight& embed,
-                          const uint32_t* ordering, int per, uint32_t* sel, float* scores_out,
-                          unsigned long long* best_key, unsigned* done, uint32_t* token_out, float* score_out,
-                          unsigned* status, cudaStream_t stream, int num_sms, int* launches) {
+cudaError_t prepare_lmhead(const float* x, int h, const float* cl, int n_cent, int k, const PackedWeight& embed,
+                           const uint32_t* ordering, int per, uint32_t* sel, float* scores_out,
+                           unsigned long long* best_key, unsigned* done, uint32_t* token_out, float* score_out,
+                           unsigned* status, int num_sms, std::vector<Launch>* out) {
   int p = 1;
   while (p < n_cent) p <<= 1;
   static std::atomic<unsigned long long> attr_set{0};  // one bit per device (setting it twice is harmless)
@@ -279,33 +279,31 @@ cudaError_t launch_lmhead(const float* x, int h, const float* cl, int n_cent, in
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set.fetch_or(1ull << dev);
   }
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(kTopkThreads);
-  cfg.dynamicSmemBytes = topk_smem(n_cent, k);
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = kUsePdl ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, cl, n_cent, p, k, sel);
-  if (launches) ++*launches;
-  if (e != cudaSuccess) return e;
+  Launch a;
+  a.fn = reinterpret_cast<const void*>(topk_kernel);
+  a.grid = dim3(1);
+  a.block = dim3(kTopkThreads);
+  a.smem = topk_smem(n_cent, k);
+  if (kUsePdl) a.allow_early_start();
+  if (!a.set_args(cl, n_cent, p, k, sel)) return cudaErrorMemoryAllocation;
 
   const int rows = k * per;
   const int warps_per_cta = kScoreThreads / 32;
   int grid = (rows + warps_per_cta - 1) / warps_per_cta;
   if (grid > 4 * num_sms) grid = 4 * num_sms;
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kScoreThreads);
-  cfg.dynamicSmemBytes = (size_t)h * sizeof(float);
-  e = cudaLaunchKernelEx(&cfg, cluster_score_kernel, x, h, reinterpret_cast<const uint16_t*>(embed.quants),
-                         (int64_t)embed.n_in_pad, ordering, (int64_t)embed.n_out, (const uint32_t*)sel, k, per,
-                         scores_out, best_key, done, token_out, score_out, status);
-  if (launches) ++*launches;
-  return e;
+  Launch b;
+  b.fn = reinterpret_cast<const void*>(cluster_score_kernel);
+  b.grid = dim3(grid);
+  b.block = dim3(kScoreThreads);
+  b.smem = (size_t)h * sizeof(float);
+  if (kUsePdl) b.allow_early_start();
+  if (!b.set_args(x, h, reinterpret_cast<const uint16_t*>(embed.quants), (int64_t)embed.n_in_pad, ordering,
+                  (int64_t)embed.n_out, (const uint32_t*)sel, k, per, scores_out, best_key, done, token_out,
+                  score_out, status))
+    return cudaErrorMemoryAllocation;
+  out->push_back(a);
+  out->push_back(b);
+  return cudaSuccess;
 }
 
 }  // namespace il

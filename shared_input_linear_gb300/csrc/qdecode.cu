@@ -1,0 +1,620 @@
+// qdecode.cu -- grouped decode kernel for Q8 / Q4 weights at small token counts
+// (t <= 8 per launch).
+//
+// For every job j of a batch over one shared x (oxinfer 0.0.0 src/gpu.rs, struct
+// `Job` and `Backend::matmul`):
+//     y_j[t][o] = sum_i x[t][i] * fp32(d_j[o][i / 32] * q_j[o][i])
+//
+// Design (GB300):
+//  * Rows of all jobs are cut into tiles of 16 (a pair of 8-row groups); every
+//    (tile, chunk) of a packed Q8/Q4 weight is one contiguous record of quants and
+//    scales (il_internal.cuh).  Each weight byte crosses HBM once.
+//  * The records stream into shared memory by bulk copies (cp.async.bulk,
+//    completion counted on an mbarrier).  Every warp owns a ring of stages, one
+//    record each, and refills a stage as soon as it has consumed it, so the bytes
+//    in flight per SM are set by the ring depth, not by registers.
+//  * Dot products run on the tensor cores (mma.m16n8k16, fp16 in, fp32
+//    accumulate).  The 16 weight rows of a record are the A operand, decoded in
+//    registers to exact fp16 integers (one byte permute or LOP3 and one fp16x2
+//    subtract per pair); x is the B operand, its tokens the 8 columns, split into
+//    an fp16 high part and the fp16 rounding of the remainder (about 22
+//    significant bits): side by side in the columns for t <= 4 (one MMA per 16
+//    columns of K), as two chained MMAs for t <= 8.  The fp32 scale of each
+//    32-block multiplies the fp32 partial of that block.
+//  * x is staged once per CTA in shared memory, already as B fragments, only for
+//    the lanes whose token exists (4 t bytes per column), scaled per token by a
+//    power of two so that fp16 holds it (undone on the partial sums).
+//  * Work: the CTAs of a K split of C take the same tiles with different K
+//    slices; inside a CTA, warps stand in a grid of wr row tiles x wk parts of
+//    the slice (wk = 1: a warp owns whole tiles).  There is no CTA-wide barrier
+//    in the stream: the last of the wk warps to finish a tile adds the parts'
+//    partial sums in part order (a generation count per partial-sum slot keeps a
+//    warp that runs ahead from overwriting a slot before it is summed), and with
+//    C > 1 the last CTA to finish a tile adds the C slices' sums from a global
+//    workspace in slice order.  Results are deterministic.
+//  * Every wait is bounded; a wait that gives up records a code in the device
+//    status word, raises a CTA abort flag, and the warps finish without waiting,
+//    then drain the copies still in flight.
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "il_internal.cuh"
+#include "il_ptx.cuh"
+
+namespace il {
+namespace {
+
+constexpr int kQWarps = 16;
+constexpr int kQThreads = kQWarps * 32;
+constexpr int kMaxQStages = 12;
+constexpr int kSlotRounds = 2;          // partial-sum slots per warp row: rounds a warp may run ahead
+constexpr unsigned kStQDecode = 0x10;   // a wait for a record gave up
+constexpr unsigned kStQSlot = 0x20;     // a wait for a free partial-sum slot gave up
+
+struct QJob {
+  const uint8_t* w;    // records
+  float* y;            // [t][n_out], or h [t][n_out / 2] when glu
+  int32_t n_out;       // packed rows
+  int32_t tile_begin;  // first global 16-row tile of this job
+  int32_t glu;
+  int32_t pad_;
+};
+
+struct QParams {
+  const float* x;
+  unsigned* status;
+  float* ws;           // C > 1: per (tile, slice) sums [tile][C][TT][16]
+  unsigned* counters;  // C > 1: arrivals per tile, zero before the launch
+  int t;               // tokens of this launch, 1..8
+  int x_row_stride;    // elements between token rows of x
+  int n_in;
+  int n_chunks;        // chunks over n_in_pad
+  int slices;          // C: CTAs that split K for one tile
+  int cps;             // chunks per slice
+  int wr, wk;          // warp grid: wr row tiles at a time x wk parts of the slice (wr * wk = 16)
+  int stages;          // ring stages per warp
+  int total_tiles;
+  int n_jobs;
+  int stall;           // failure-detection test: issue no copies, so the waits run out
+  QJob jobs[kMaxDecodeJobs];
+};
+
+template <int FMT>
+struct QF {
+  static constexpr int CK = chunk_k(FMT);            // columns per chunk
+  static constexpr int SLOTS = CK / 16;              // 16-column MMA slots per chunk
+  static constexpr int BLOCKS = blocks_per_chunk(FMT);
+  static constexpr int SB = chunk_scale_bytes(FMT);  // scale bytes of one group in a record
+  static constexpr int RS = record_bytes(FMT);
+};
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
+
+__device__ __forceinline__ int find_tile_job(const QParams& p, int tile) {
+  int j = p.n_jobs - 1;
+  while (j > 0 && p.jobs[j].tile_begin > tile) --j;
+  return j;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// x exponent of a token from the bits of its largest |x| (a non-negative float):
+// 2^-e brings that value into [2^13, 2^14); e stays in [-126, 114] so both powers
+// of two are normal floats.
+__device__ __forceinline__ int x_exponent(unsigned max_bits) {
+  const float m = __uint_as_float(max_bits);
+  return m > 0.f ? max(-126, min(114, ilogbf(m) - 13)) : 0;
+}
+
+// One record: 16 rows x CK columns against the x fragments of that chunk
+// (xb: this lane's fragment of the chunk's first slot, xstep bytes per slot).
+// acc: (row g, token col 2q), (row g, col 2q+1), (row g+8, col 2q), (row g+8, col 2q+1).
+template <int FMT, int TT>
+__device__ __forceinline__ void consume_record(const uint8_t* st, int lane, int g, const uint8_t* xb, int xstep,
+                                               bool xvalid, float (&acc)[4]) {
+  using F = QF<FMT>;
+  const uint4 q0 = *reinterpret_cast<const uint4*>(st + lane * 16);        // rows 0..7 (group 2p)
+  const uint4 q1 = *reinterpret_cast<const uint4*>(st + 512 + lane * 16);  // rows 8..15 (group 2p+1)
+  float d0[F::BLOCKS], d1[F::BLOCKS];
+  if (FMT == IL_Q8) {
+    const float2 a = *reinterpret_cast<const float2*>(st + 1024 + g * 8);
+    const float2 b = *reinterpret_cast<const float2*>(st + 1024 + F::SB + g * 8);
+    d0[0] = a.x; d0[1 % F::BLOCKS] = a.y;
+    d1[0] = b.x; d1[1 % F::BLOCKS] = b.y;
+  } else {
+    const float4 a = *reinterpret_cast<const float4*>(st + 1024 + g * 16);
+    const float4 b = *reinterpret_cast<const float4*>(st + 1024 + F::SB + g * 16);
+    d0[0] = a.x; d0[1 % F::BLOCKS] = a.y; d0[2 % F::BLOCKS] = a.z; d0[3 % F::BLOCKS] = a.w;
+    d1[0] = b.x; d1[1 % F::BLOCKS] = b.y; d1[2 % F::BLOCKS] = b.z; d1[3 % F::BLOCKS] = b.w;
+  }
+#pragma unroll
+  for (int b = 0; b < F::BLOCKS; ++b) {
+    // B fragments of slots 2b and 2b+1: {high k-pair lo, hi} (and the low parts of x for TT = 8)
+    uint4 xa = make_uint4(0, 0, 0, 0), xc = make_uint4(0, 0, 0, 0);
+    if (xvalid) {
+      if (TT == 8) {
+        xa = *reinterpret_cast<const uint4*>(xb + (2 * b) * xstep);
+        xc = *reinterpret_cast<const uint4*>(xb + (2 * b + 1) * xstep);
+      } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(xb + (2 * b) * xstep);
+        const uint2 v = *reinterpret_cast<const uint2*>(xb + (2 * b + 1) * xstep);
+        xa = make_uint4(u.x, u.y, 0, 0);
+        xc = make_uint4(v.x, v.y, 0, 0);
+      }
+    }
+    uint32_t A0[4], A1[4];  // slots 2b and 2b+1: {row g k-pair lo, row g+8 lo, row g hi, row g+8 hi}
+    if (FMT == IL_Q8) {
+      uint32_t p01, p23, r01, r23;
+      q8_word_to_f16x2(word_of(q0, 2 * b), p01, p23);
+      q8_word_to_f16x2(word_of(q1, 2 * b), r01, r23);
+      A0[0] = p01; A0[1] = r01; A0[2] = p23; A0[3] = r23;
+      q8_word_to_f16x2(word_of(q0, 2 * b + 1), p01, p23);
+      q8_word_to_f16x2(word_of(q1, 2 * b + 1), r01, r23);
+      A1[0] = p01; A1[1] = r01; A1[2] = p23; A1[3] = r23;
+    } else {
+      uint32_t pa[4], pb[4];
+      q4_word_to_f16x2(word_of(q0, b), pa);
+      q4_word_to_f16x2(word_of(q1, b), pb);
+      A0[0] = pa[0]; A0[1] = pb[0]; A0[2] = pa[1]; A0[3] = pb[1];
+      A1[0] = pa[2]; A1[1] = pb[2]; A1[2] = pa[3]; A1[3] = pb[3];
+    }
+    float t4[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_f16(t4, A0, xa.x, xa.y);
+    if (TT == 8) mma_f16(t4, A0, xa.z, xa.w);
+    mma_f16(t4, A1, xc.x, xc.y);
+    if (TT == 8) mma_f16(t4, A1, xc.z, xc.w);
+    acc[0] = fmaf(d0[b], t4[0], acc[0]);
+    acc[1] = fmaf(d0[b], t4[1], acc[1]);
+    acc[2] = fmaf(d1[b], t4[2], acc[2]);
+    acc[3] = fmaf(d1[b], t4[3], acc[3]);
+  }
+}
+
+// Stores one summed value -- token tk, row `row` of `tile` -- into its job's y.
+// Called by every lane of the warp (the gate/up pairing reads the neighbouring
+// row's sum from the next lane).
+__device__ __forceinline__ void store_item(const QParams& p, int tile, bool have, float v, int row, int tk) {
+  const float up = __shfl_down_sync(0xffffffffu, v, 1);  // row + 1 of the same token
+  if (!have || tk >= p.t) return;
+  const QJob& jb = p.jobs[find_tile_job(p, tile)];
+  const int r = (tile - jb.tile_begin) * 16 + row;
+  if (r >= jb.n_out) return;
+  if (jb.glu) {
+    // rows 2i and 2i+1 are gate and up of output column i
+    if ((row & 1) == 0) jb.y[(size_t)tk * (jb.n_out >> 1) + (r >> 1)] = gelu_mul(v, up);
+  } else {
+    jb.y[(size_t)tk * jb.n_out + r] = v;
+  }
+}
+
+template <int FMT, int TT>
+__global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_constant__ QParams p) {
+  using F = QF<FMT>;
+  constexpr int RS = F::RS;
+  constexpr int XL = TT == 8 ? 16 : 8;  // bytes of one lane's B fragment per slot
+  constexpr int NI = TT / 2;            // summed items per lane: TT tokens x 16 rows over 32 lanes
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int g = lane >> 2;  // A rows g and g+8 of the tile; B column (token slot)
+  const int q = lane & 3;
+
+  const int rank = blockIdx.x % p.slices;
+  const int stream = blockIdx.x / p.slices;
+  const int nstreams = gridDim.x / p.slices;
+  const int D = p.stages;
+  const int wr_i = warp / p.wk, wk_i = warp - (warp / p.wk) * p.wk;
+  // this CTA's K slice and this warp's even share of it (chunk indices from cb)
+  const int cb = rank * p.cps;
+  const int ns = max(0, min(p.cps, p.n_chunks - cb));
+  const int c0 = (wk_i * ns) / p.wk;
+  const int cnt = ((wk_i + 1) * ns) / p.wk - c0;
+  const int tg_total = (p.total_tiles + p.wr - 1) / p.wr;
+  const int rounds = stream < tg_total ? (tg_total - stream + nstreams - 1) / nstreams : 0;
+
+  // shared memory: x fragments | rings | partial sums | slot counts | barriers
+  const int xslot = 64 * p.t;  // bytes per 16-column slot of x fragments
+  const size_t xs_bytes = ((size_t)p.cps * F::SLOTS * xslot + 127) & ~(size_t)127;
+  uint8_t* xs = smem;
+  uint8_t* ring = smem + xs_bytes + (size_t)warp * D * RS;
+  float* part = reinterpret_cast<float*>(smem + xs_bytes + (size_t)kQWarps * D * RS);  // [NB][16 warps][TT][16]
+  int* cnt_s = reinterpret_cast<int*>(part + kSlotRounds * kQWarps * TT * 16);           // [NB][16 rows of warps]
+  int* gen_s = cnt_s + kSlotRounds * kQWarps;                                            // [NB][16]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gen_s + kSlotRounds * kQWarps) + warp * kMaxQStages;
+  unsigned* tok_max = reinterpret_cast<unsigned*>(reinterpret_cast<uint64_t*>(gen_s + kSlotRounds * kQWarps) +
+                                                  kQWarps * kMaxQStages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tok_max + 8);
+
+  if (lane == 0)
+    for (int s = 0; s < D; ++s) mbar_init(smem_u32(&bars[s]), 1);
+  if (threadIdx.x < kSlotRounds * kQWarps) {
+    cnt_s[threadIdx.x] = 0;
+    gen_s[threadIdx.x] = 0;
+  }
+  if (threadIdx.x < 8) tok_max[threadIdx.x] = 0u;
+  if (threadIdx.x == 0) *abort_flag = 0;
+  if (lane == 0) mbar_init_fence();
+  __syncthreads();
+
+  // ---- load cursor (lane 0): this warp's records in consumption order, (round,
+  // chunk) with the chunk fastest; a row slot whose tile lies past the last one
+  // has no records (only the last rounds can).
+  int l_round = 0, l_cc = 0, l_stage = 0, issued = 0;
+  const uint8_t* l_src = nullptr;
+  const uint64_t policy = policy_evict_first();
+  auto tile_records = [&](int round) -> const uint8_t* {
+    if (round >= rounds) return nullptr;
+    const int tile = (stream + round * nstreams) * p.wr + wr_i;
+    if (tile >= p.total_tiles) return nullptr;
+    const QJob& jb = p.jobs[find_tile_job(p, tile)];
+    return jb.w + ((size_t)(tile - jb.tile_begin) * p.n_chunks + cb + c0) * RS;
+  };
+  if (lane == 0 && cnt > 0) l_src = tile_records(0);
+  auto issue_next = [&]() {
+    if (l_src == nullptr) return;
+    const uint32_t bar = smem_u32(&bars[l_stage]);
+    mbar_expect_tx(bar, RS);
+    if (!p.stall) bulk_g2s_hint(smem_u32(ring + (size_t)l_stage * RS), l_src + (size_t)l_cc * RS, RS, bar, policy);
+    ++issued;
+    if (++l_stage == D) l_stage = 0;
+    if (++l_cc == cnt) {
+      l_cc = 0;
+      l_src = tile_records(++l_round);
+    }
+  };
+  // Weights do not depend on the previous kernel: start streaming before waiting for it.
+  if (lane == 0)
+    for (int s = 0; s < D; ++s) issue_next();
+  grid_dep_wait();
+  // the next kernel may now be scheduled; it waits for this one before touching x or y
+  grid_dep_launch();
+
+  // ---- x of this CTA's slice as B fragments, token by token scaled by 2^-e(tok)
+  // so that its largest |x| in the slice lies in [2^13, 2^14).  Fragment layout:
+  // [slot][compact lane] -- TT = 8: lanes 4 tok + q hold {high, low} parts (16 bytes);
+  // TT = 4: lanes 8 tok + 4 h + q hold the high (h = 0) or low (h = 1) part (8 bytes).
+  const int cols = ns * F::CK;
+  for (int tk = 0; tk < p.t; ++tk) {
+    const float* xrow = p.x + (size_t)tk * p.x_row_stride + (size_t)cb * F::CK;
+    float mx = 0.f;
+    for (int c4 = threadIdx.x; c4 < cols / 4; c4 += kQThreads)
+      if (cb * F::CK + 4 * c4 < p.n_in) {
+        const float4 v = *reinterpret_cast<const float4*>(xrow + 4 * c4);
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0 && mx > 0.f) atomicMax(&tok_max[tk], __float_as_uint(mx));  // non-negative: bits order as values
+  }
+  __syncthreads();
+  const int lanes_per_slot = (TT == 8 ? 4 : 8) * p.t;
+  for (int e = threadIdx.x; e < ns * F::SLOTS * lanes_per_slot; e += kQThreads) {
+    const int sl = e / lanes_per_slot, ci = e - (e / lanes_per_slot) * lanes_per_slot;
+    const int tk = TT == 8 ? ci >> 2 : ci >> 3;
+    const int qq = ci & 3;
+    const int col = cb * F::CK + (sl / F::SLOTS) * F::CK + 16 * (sl % F::SLOTS) + 4 * qq;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (col < p.n_in) v = *reinterpret_cast<const float4*>(p.x + (size_t)tk * p.x_row_stride + col);
+    const float xsc = ldexpf(1.0f, -x_exponent(tok_max[tk]));
+    const __half2 h01 = __floats2half2_rn(v.x * xsc, v.y * xsc);
+    const __half2 h23 = __floats2half2_rn(v.z * xsc, v.w * xsc);
+    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+    const __half2 l01 = __floats2half2_rn(v.x * xsc - f01.x, v.y * xsc - f01.y);
+    const __half2 l23 = __floats2half2_rn(v.z * xsc - f23.x, v.w * xsc - f23.y);
+    uint8_t* dst = xs + (size_t)sl * xslot + ci * XL;
+    if (TT == 8) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(h2_bits(h01), h2_bits(h23), h2_bits(l01), h2_bits(l23));
+    } else {
+      const bool low = (ci >> 2) & 1;
+      *reinterpret_cast<uint2*>(dst) = low ? make_uint2(h2_bits(l01), h2_bits(l23)) : make_uint2(h2_bits(h01), h2_bits(h23));
+    }
+  }
+  __syncthreads();
+  // this lane's B fragment: column g is token g (TT = 8) or the high / low part of token g % 4
+  const int my_tok = TT == 8 ? g : (g & 3);
+  const bool xvalid = my_tok < p.t;
+  const int my_ci = TT == 8 ? 4 * g + q : 8 * (g & 3) + 4 * (g >> 2) + q;
+  const uint8_t* xlane = xs + my_ci * XL;
+  // scale back of the partials: this lane's D columns are tokens 2q and 2q+1
+  // (for t <= 4, lanes q < 2 after folding the low-part columns in)
+  const int tq0 = TT == 8 ? 2 * q : 2 * (q & 1), tq1 = tq0 + 1;
+  const float ys0 = ldexpf(1.0f, x_exponent(tok_max[tq0]));
+  const float ys1 = ldexpf(1.0f, x_exponent(tok_max[tq1]));
+
+  int c_stage = 0;
+  uint32_t c_phase = 0;
+  int consumed = 0;
+  bool ok = true;
+  for (int r = 0; r < rounds; ++r) {
+    const int tile = (stream + r * nstreams) * p.wr + wr_i;
+    if (tile >= p.total_tiles) break;  // same for the whole row of warps, and for every later round
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int cc = 0; cc < cnt && ok; ++cc) {
+      const uint32_t bar = smem_u32(&bars[c_stage]);
+      ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar, c_phase, abort_flag, p.status, kStQDecode));
+      if (!ok) break;
+      consume_record<FMT, TT>(ring + (size_t)c_stage * RS, lane, g, xlane + (size_t)(c0 + cc) * F::SLOTS * xslot,
+                              xslot, xvalid, acc);
+      ++consumed;
+      // every lane's reads of this stage are done before the copy that refills it
+      __syncwarp();
+      if (lane == 0) issue_next();
+      if (++c_stage == D) {
+        c_stage = 0;
+        c_phase ^= 1;
+      }
+    }
+    if (TT == 4) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 2);  // high + low columns
+    }
+    // ---- this warp's partial -> its slot, once the slot's previous use is summed
+    const int sr = r % kSlotRounds;
+    const int slot = sr * kQWarps + wr_i;
+    if (r >= kSlotRounds) {
+      const int want = r / kSlotRounds;
+      volatile int* gs = gen_s + slot;
+      if (*gs < want) {
+        const long long start = clock64();
+        while (*gs < want) {
+          if (*abort_flag) break;
+          if ((unsigned long long)(clock64() - start) > kWaitLimitCycles) {
+            *abort_flag = 1;
+            atomicOr(p.status, kStQSlot);
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      __threadfence_block();
+    }
+    float* pw = part + (size_t)((sr * kQWarps + warp) * TT) * 16;
+    if (TT == 8 || q < 2) {
+      pw[(2 * q) * 16 + g] = acc[0] * ys0;
+      pw[(2 * q + 1) * 16 + g] = acc[1] * ys1;
+      pw[(2 * q) * 16 + g + 8] = acc[2] * ys0;
+      pw[(2 * q + 1) * 16 + g + 8] = acc[3] * ys1;
+    }
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(&cnt_s[slot], 1) == p.wk - 1;
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+    // ---- the last of the tile's wk parts: sum them in part order, (token, row)
+    // items with rows fastest
+    __threadfence_block();
+    const float* pr = part + (size_t)((sr * kQWarps + wr_i * p.wk) * TT) * 16;
+    float v[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int e = lane + 32 * i;
+      float s = 0.f;
+#pragma unroll
+      for (int k = 0; k < kQWarps; ++k)
+        if (k < p.wk) s += pr[(size_t)k * TT * 16 + e];
+      v[i] = s;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      cnt_s[slot] = 0;
+      __threadfence_block();
+      atomicAdd(&gen_s[slot], 1);  // the slot may be written again
+    }
+    if (p.slices > 1) {
+      // ---- then over the C slices, through the global workspace: the last CTA to
+      // arrive adds them in slice order
+      float* wsp = p.ws + ((size_t)tile * p.slices + rank) * TT * 16;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) __stcg(wsp + lane + 32 * i, v[i]);
+      __threadfence();
+      __syncwarp();
+      int lastc = 0;
+      if (lane == 0) lastc = atomicAdd(p.counters + tile, 1u) == (unsigned)(p.slices - 1);
+      if (!__shfl_sync(0xffffffffu, lastc, 0)) continue;
+      __threadfence();
+      const float* wt = p.ws + (size_t)tile * p.slices * TT * 16;
+#pragma unroll
+      for (int i = 0; i < NI; ++i) {
+        float s = 0.f;
+        for (int c = 0; c < p.slices; ++c) s += __ldcg(wt + (size_t)c * TT * 16 + lane + 32 * i);
+        v[i] = s;
+      }
+      if (lane == 0) p.counters[tile] = 0u;  // zero again for the next launch
+    }
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int e = lane + 32 * i;
+      store_item(p, tile, true, v[i], e & 15, e >> 4);
+    }
+  }
+  // after a wait gave up: let the copies this warp still has in flight land
+  // before the CTA's shared memory is released
+  if (!ok && lane == 0 && !p.stall) {
+    int s = c_stage;
+    uint32_t ph = c_phase;
+    for (int k = consumed; k < issued; ++k) {
+      mbar_wait_for(smem_u32(&bars[s]), ph, kWaitLimitCycles / 8);
+      if (++s == D) {
+        s = 0;
+        ph ^= 1;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side: plan + launch
+// ---------------------------------------------------------------------------
+using QKernelFn = void (*)(QParams);
+
+QKernelFn select_q(int fmt, int TT) {
+  if (fmt == IL_Q8) return TT == 8 ? qdecode_kernel<IL_Q8, 8> : qdecode_kernel<IL_Q8, 4>;
+  if (fmt == IL_Q4) return TT == 8 ? qdecode_kernel<IL_Q4, 8> : qdecode_kernel<IL_Q4, 4>;
+  return nullptr;
+}
+
+size_t q_x_bytes(int fmt, int t, int cps) {
+  return ((size_t)cps * (chunk_k(fmt) / 16) * 64 * t + 127) & ~(size_t)127;
+}
+
+// Shared memory besides the x fragments and the rings.
+size_t q_fixed_bytes(int TT) {
+  return (size_t)kSlotRounds * kQWarps * TT * 16 * sizeof(float) + 2 * (size_t)kSlotRounds * kQWarps * sizeof(int) +
+         (size_t)kQWarps * kMaxQStages * 8 + 8 * sizeof(unsigned) + 16;
+}
+
+// Dynamic shared memory a CTA may take, once per device (the kernels' attribute
+// is raised to it on first use).
+int q_smem_limit(int dev) {
+  static std::mutex mu;
+  static std::map<int, int> limit;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = limit.find(dev);
+  if (it != limit.end()) return it->second;
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+  for (int fmt = IL_Q8; fmt <= IL_Q4; ++fmt)
+    for (int TT = 4; TT <= 8; TT += 4)
+      if (cudaFuncSetAttribute(select_q(fmt, TT), cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
+        return 0;
+  limit[dev] = optin;
+  return optin;
+}
+
+struct QPlan {
+  int C = 0, cps = 0, wr = 0, wk = 0, stages = 0, streams = 0;
+  size_t smem = 0, ws_bytes = 0;
+};
+
+// The launch plan: K split over C CTAs, the warp grid (wr row tiles x wk parts),
+// the ring depth that fills the shared memory left by the x fragments.  Scored
+// by how evenly whole rounds of tile groups fill the SMs (a part-full last round
+// idles SMs), by how many warps a round keeps busy, and by the records a warp
+// streams per round (each round ends with a partial sum).  ws_room: split
+// workspace available (SIZE_MAX: any).
+bool plan_q(int fmt, int t, int n_chunks, int total_tiles, int num_sms, int smem_limit, size_t ws_room, QPlan* out) {
+  const int TT = t <= 4 ? 4 : 8;
+  const double work = (double)total_tiles * n_chunks;
+  double best = -1.0;
+  for (int c = 1; c <= 8 && c <= n_chunks; ++c) {
+    const int cps = (n_chunks + c - 1) / c;
+    if ((n_chunks + cps - 1) / cps != c) continue;
+    size_t ws = 0;
+    if (c > 1) {
+      if (total_tiles > kSplitCounters) continue;
+      ws = kSplitCounterBytes + (size_t)total_tiles * c * TT * 16 * sizeof(float);
+      if (ws > ws_room) continue;
+    }
+    const size_t fixed = q_x_bytes(fmt, t, cps) + q_fixed_bytes(TT);
+    if (fixed >= (size_t)smem_limit) continue;
+    int stages = (int)(((size_t)smem_limit - fixed) / ((size_t)kQWarps * record_bytes(fmt)));
+    if (stages > kMaxQStages) stages = kMaxQStages;
+    if (stages < 3) continue;
+    const int streams = num_sms / c;
+    for (int wk = kQWarps; wk >= 1; wk /= 2) {
+      const int wr = kQWarps / wk;
+      const int cpw = (cps + wk - 1) / wk;
+      const int tg = (total_tiles + wr - 1) / wr;
+      const int used = tg < streams ? tg : streams;
+      const int rounds = (tg + used - 1) / used;
+      const double eff = work / ((double)num_sms * rounds * wr * cps);
+      const int busy = (cps < wk ? cps : wk) * wr;  // warps with records in a full round
+      const double score = eff * (1.0 - 0.03 * (c - 1)) * (busy >= 8 ? 1.0 : busy / 8.0) * cpw / (cpw + 0.5);
+      if (score > best) {
+        best = score;
+        out->C = c;
+        out->cps = cps;
+        out->wr = wr;
+        out->wk = wk;
+        out->stages = stages;
+        out->streams = used;
+        out->smem = fixed + (size_t)kQWarps * stages * record_bytes(fmt);
+        out->ws_bytes = ws;
+      }
+    }
+  }
+  return best > 0.0;
+}
+
+}  // namespace
+
+size_t qdecode_workspace_bytes(int fmt, const DecodeParams& d, int num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const int limit = q_smem_limit(dev);
+  QPlan pl;
+  if (limit <= 0 || !plan_q(fmt, d.t, d.n_chunks, d.total_groups / 2, num_sms, limit, SIZE_MAX, &pl)) return 0;
+  return pl.ws_bytes;
+}
+
+cudaError_t prepare_qdecode(int fmt, const DecodeParams& d, int num_sms, unsigned* status, void* ws, size_t ws_bytes,
+                            Launch* out) {
+  if (fmt != IL_Q8 && fmt != IL_Q4) return cudaErrorInvalidValue;
+  if (d.t < 1 || d.t > 8 || d.n_jobs < 1 || d.n_jobs > kMaxDecodeJobs || (d.total_groups & 1)) return cudaErrorInvalidValue;
+  const int TT = d.t <= 4 ? 4 : 8;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int limit = q_smem_limit(dev);
+  if (limit <= 0) return cudaErrorInvalidValue;
+  QPlan pl;
+  if (!plan_q(fmt, d.t, d.n_chunks, d.total_groups / 2, num_sms, limit, ws != nullptr ? ws_bytes : 0, &pl))
+    return cudaErrorInvalidValue;
+
+  QParams p;
+  memset(&p, 0, sizeof p);
+  p.x = d.x;
+  p.status = status;
+  if (pl.C > 1) {
+    p.counters = static_cast<unsigned*>(ws);
+    p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kSplitCounterBytes);
+  }
+  p.t = d.t;
+  p.x_row_stride = d.x_row_stride;
+  p.n_in = d.n_in;
+  p.n_chunks = d.n_chunks;
+  p.slices = pl.C;
+  p.cps = pl.cps;
+  p.wr = pl.wr;
+  p.wk = pl.wk;
+  p.stages = pl.stages;
+  p.total_tiles = d.total_groups / 2;
+  p.n_jobs = d.n_jobs;
+  for (int j = 0; j < d.n_jobs; ++j) {
+    if (d.jobs[j].group_begin & 1) return cudaErrorInvalidValue;
+    p.jobs[j].w = d.jobs[j].w;
+    p.jobs[j].y = d.jobs[j].y;
+    p.jobs[j].n_out = d.jobs[j].n_out;
+    p.jobs[j].tile_begin = d.jobs[j].group_begin / 2;
+    p.jobs[j].glu = d.jobs[j].glu;
+  }
+  const char* stall = getenv("IL_TEST_STALL_TMA_PRODUCER");
+  p.stall = (stall != nullptr && stall[0] == '1') ? 1 : 0;
+
+  Launch& L = *out;
+  L = Launch();
+  L.fn = reinterpret_cast<const void*>(select_q(fmt, TT));
+  L.grid = dim3(pl.streams * pl.C);
+  L.block = dim3(kQThreads);
+  L.smem = pl.smem;
+  // one CTA per SM at most: an early start behind the previous kernel takes
+  // SMs as they free up and streams this batch's weights meanwhile
+  if (kUsePdl) L.allow_early_start();
+  if (!L.set_args(p)) return cudaErrorMemoryAllocation;
+  return cudaSuccess;
+}
+
+}  // namespace il

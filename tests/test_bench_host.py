@@ -79,3 +79,28 @@ def test_reference_arm_other_ranks_exit_quietly():
                           "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
                          timeout=120, cwd=ROOT, env=env)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_reference_arm_matches_the_headline_config():
+    import bench
+    # both arms describe the same workload (the driver compares the two lines) and
+    # the reference arm runs the warm-up it was asked for
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "1"], capture_output=True, text=True,
+                         timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["config"] == bench.headline_config(2, 1)
+    assert line["warmup"] == 1 and line["steps"] == 2
+    assert line["cpu_baseline"]["cores"] == bench.host_threads()
+
+
+def test_oracle_config_time_on_a_sample():
+    import bench
+    import workloads as wl
+    # the per-config oracle time comes from a bounded sample scaled to the batch
+    inp = wl.make_batch(512, (64, 32), 100, "q4", seed=3)
+    ms, frac = bench.oracle_config_ms(inp, threads=2, budget_macs=4e5)
+    assert ms > 0 and 0 < frac < 1
+    ms_full, frac_full = bench.oracle_config_ms(wl.make_batch(64, (16,), 2, "bf16", seed=3), threads=2)
+    assert frac_full == 1.0 and ms_full > 0

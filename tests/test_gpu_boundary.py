@@ -227,3 +227,123 @@ def test_bounded_wait_reports_timeout():
                          capture_output=True, text=True, timeout=300)
     assert "CODE -7" in out.stdout, out.stdout + out.stderr
     assert "AFTER True" in out.stdout, out.stdout + out.stderr
+
+
+_STALL_SCRIPT = r"""
+import os, sys
+sys.path.insert(0, {root!r})
+import numpy as np
+import torch
+torch.cuda.set_device(0)
+import shared_input_linear_gb300 as sil
+import workloads as wl
+import oracle
+fmt, t, entry = {fmt!r}, {t!r}, {entry!r}
+b = wl.make_batch(512, (96, 40), t, fmt, seed=4)
+ws = [sil.upload_weight(f, buf, n, 512) for f, buf, n in b.jobs]
+x = torch.from_numpy(b.x).cuda()
+ys = [torch.zeros(t, n, device="cuda") for _, _, n in b.jobs]
+jobs = [(w, n, y.data_ptr()) for w, (_, _, n), y in zip(ws, b.jobs, ys)]
+call = sil.matmul_batch_ptr if entry == "batch" else sil.matmul_batch_noalloc_ptr
+s = torch.cuda.current_stream().cuda_stream
+call(x.data_ptr(), t, 512, jobs, s)      # a warm call: the entry point is set up
+torch.cuda.synchronize()
+os.environ["IL_TEST_STALL_TMA_PRODUCER"] = "1"
+call(x.data_ptr(), t, 512, jobs, s)      # the kernel's waits give up after ~1 s
+try:
+    sil.check_device_status()
+    print("NO_TIMEOUT")
+except sil.ILError as e:
+    print("CODE", e.code)
+del os.environ["IL_TEST_STALL_TMA_PRODUCER"]
+for y in ys:
+    y.fill_(float("nan"))
+call(x.data_ptr(), t, 512, jobs, s)      # the context is still usable
+torch.cuda.synchronize()
+sil.check_device_status()
+ok = True
+for (f, buf, n), y in zip(b.jobs, ys):
+    y_ref, mag = oracle.linear(f, buf, n, 512, b.x)
+    ok &= oracle.check(y.cpu().numpy(), y_ref, mag)[0]
+print("AFTER", ok)
+"""
+
+
+@pytest.mark.parametrize("fmt,t,entry", [
+    ("q4", 1, "batch"),      # Q8/Q4 decode kernel: its bulk-copy waits
+    ("q8", 6, "batch"),
+    ("bf16", 16, "noalloc"),  # tensor-core kernel through the no-alloc entry point
+    ("q4", 3, "noalloc"),     # decode kernel through the no-alloc entry point
+])
+def test_stalled_copies_report_timeout(fmt, t, entry):
+    # The copies a kernel waits for are never issued (a test switch read on the
+    # host): its bounded waits give up after about a second, the code lands in
+    # the status word of that entry point, il_check_device_status reports it, and
+    # the next call on the same context is correct.
+    out = subprocess.run([sys.executable, "-c", _STALL_SCRIPT.format(root=ROOT, fmt=fmt, t=t, entry=entry)],
+                         capture_output=True, text=True, timeout=300)
+    assert "CODE -7" in out.stdout, out.stdout + out.stderr
+    assert "AFTER True" in out.stdout, out.stdout + out.stderr
+
+
+_MAPFAIL_SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r})
+import numpy as np
+import torch
+torch.cuda.set_device(0)
+import shared_input_linear_gb300 as sil
+import workloads as wl
+t, n_in = 64, 512
+b16 = wl.make_batch(n_in, (200, 72), t, "bf16", seed=5)
+b8 = wl.make_batch(n_in, (136,), t, "q8", seed=6)
+jobs = b16.jobs + b8.jobs
+ws = [sil.upload_weight(f, buf, n, n_in) for f, buf, n in jobs]
+x = torch.from_numpy(b16.x).cuda()
+ys = [torch.full((t, n), 7.0, device="cuda") for _, _, n in jobs]
+before = sil.get_stats()["launches"]
+try:
+    # tensor maps: x and two weights for the bf16 launch, then x, quants and scales
+    # for the Q8 launch; the 4th encoding fails, after the bf16 launch was prepared
+    sil.matmul_batch(x, list(zip(ws, ys)))
+    print("NO_ERROR")
+except sil.ILError as e:
+    print("CODE", e.code)
+torch.cuda.synchronize()
+print("LAUNCHES", sil.get_stats()["launches"] - before)
+print("UNTOUCHED", all(bool(torch.all(y == 7.0)) for y in ys))
+"""
+
+
+def test_failed_preparation_enqueues_nothing():
+    # A mixed bf16 + Q8 batch on the tensor-core path whose second launch cannot be
+    # prepared (the 4th tensor-map encoding of the process is made to fail): the
+    # call returns an error, launched no kernel (not even the cast of x or the bf16
+    # launch that was ready) and wrote no y.
+    env = dict(os.environ, IL_FAULT_TENSOR_MAP_FAIL_AFTER="3")
+    out = subprocess.run([sys.executable, "-c", _MAPFAIL_SCRIPT.format(root=ROOT)], env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert "CODE -6" in out.stdout, out.stdout + out.stderr
+    assert "LAUNCHES 0" in out.stdout, out.stdout + out.stderr
+    assert "UNTOUCHED True" in out.stdout, out.stdout + out.stderr
+
+
+def test_release_scratch(sil):
+    import torch
+    import oracle
+    import workloads as wl
+    s = torch.cuda.Stream()
+    b = wl.make_batch(1024, (300, 40), 64, "bf16", seed=8)
+    ws = [sil.upload_weight(f, buf, n, 1024) for f, buf, n in b.jobs]
+    x = torch.from_numpy(b.x).cuda()
+    for _ in range(2):
+        ys = [torch.full((64, n), float("nan"), device="cuda") for _, _, n in b.jobs]
+        with torch.cuda.stream(s):
+            sil.matmul_batch(x, list(zip(ws, ys)), stream=s)
+            sil.release_scratch(s)  # freed in stream order, after the batch that reads it
+        s.synchronize()
+        for (f, buf, n), y in zip(b.jobs, ys):
+            y_ref, mag = oracle.linear(f, buf, n, 1024, b.x)
+            assert oracle.check(y.cpu().numpy(), y_ref, mag)[0]
+    for w in ws:
+        w.free()

@@ -357,3 +357,57 @@ def test_full_size_sampled(sil, w, bt, t, fmt):
     ys, guards = run(sil, b)
     assert guards
     assert_parity_sampled(b, ys, what=f"{w.name}/{bt.name}")
+
+
+# ---------------------------------------------------------------------------
+# launch counts and size limits: batches that need more than one launch of a
+# kernel, and the largest n_in
+# ---------------------------------------------------------------------------
+def _launches(sil, b):
+    before = sil.get_stats()["launches"]
+    ys, guards = run(sil, b)
+    return ys, guards, sil.get_stats()["launches"] - before
+
+
+def test_twelve_gemm_jobs_two_launches(sil):
+    # 12 bf16 jobs at t = 64: one cast of x, then 8 + 4 jobs on the tensor-core kernel
+    n_outs = tuple(40 + 24 * j for j in range(12))
+    b = wl.make_batch(512, n_outs, 64, "bf16", seed=31)
+    ys, guards, launches = _launches(sil, b)
+    assert guards
+    assert launches == 3
+    assert_parity(b, ys, "12 GEMM jobs")
+
+
+def test_forty_decode_jobs_two_launches(sil):
+    # 40 bf16 jobs at t = 1: 32 + 8 jobs on the decode kernel
+    n_outs = tuple(8 + 16 * (j % 7) for j in range(40))
+    b = wl.make_batch(256, n_outs, 1, "bf16", seed=32)
+    ys, guards, launches = _launches(sil, b)
+    assert guards
+    assert launches == 2
+    assert_parity(b, ys, "40 decode jobs")
+
+
+def test_mixed_quant_formats_tensor_core(sil):
+    # one Q4 job and ten Q8 jobs at t = 24: one cast, 8 + 2 Q8 jobs and 1 Q4 job on the
+    # tensor-core kernel (Q8/Q4 dequantised in shared memory)
+    t, n_in = 24, 512
+    b4 = wl.make_batch(n_in, (200,), t, "q4", seed=33)
+    b8 = wl.make_batch(n_in, tuple(16 + 40 * j for j in range(10)), t, "q8", seed=34)
+    b = wl.BatchInputs("mixed", t, n_in, b4.x, b4.jobs + b8.jobs)
+    ys, guards, launches = _launches(sil, b)
+    assert guards
+    assert launches == 4
+    assert_parity(b, ys, "Q4 + 10 Q8")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+@pytest.mark.parametrize("t", [1, 8, 40])
+def test_largest_n_in(sil, fmt, t):
+    # n_in = 32768, the documented limit: the decode kernel splits K over a cluster
+    # of 8 CTAs, the tensor-core kernel walks 512 k-blocks
+    b = wl.make_batch(32768, (72, 24), t, fmt, seed=35 + t)
+    ys, guards = run(sil, b)
+    assert guards
+    assert_parity(b, ys, "n_in 32768")

@@ -539,3 +539,16 @@ def test_planted_mistake_is_caught(tmp_path, name):
             failed.append(pin.__name__)
     assert failed, f"no pin caught the planted mistake {name}"
     shutil.rmtree(tmp_path, ignore_errors=True)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+@pytest.mark.parametrize("threads", [1, 3, 8])
+def test_threaded_leg_is_the_same_computation(orc, fmt, threads):
+    # The timing leg splits each job's rows over host threads; every element must
+    # come out bit for bit as in the single-threaded oracle (same dequantisation,
+    # same summation order), including a row count that does not divide evenly.
+    b = wl.make_batch(256, (37,), 3, fmt, seed=threads)
+    f, buf, n = b.jobs[0]
+    y1, m1 = orc.linear(f, buf, n, 256, b.x)
+    y2, m2 = orc.linear_threads(f, buf, n, 256, b.x, threads)
+    assert np.array_equal(y1, y2) and np.array_equal(m1, m2)

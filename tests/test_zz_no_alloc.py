@@ -71,3 +71,38 @@ def test_noalloc_rejects_more_than_its_scratch(sil):
     torch.cuda.synchronize()
     assert bool(torch.all(y == 7.0))
     w.free()
+
+
+def test_noalloc_allocates_no_device_memory(sil):
+    # The property the entry point exists for: after one call of each path (which
+    # loads the kernels and sets the device up), further calls leave the device's
+    # free memory unchanged.  Only no-alloc calls run here, so no scratch of
+    # il_matmul_batch can hide an allocation.
+    import torch
+    cases = [("bf16", 40, 1024, (300, 64)),   # tensor-core path, bf16
+             ("q8", 24, 512, (136,)),         # tensor-core path, Q8 dequantised in shared memory
+             ("bf16", 3, 1024, (300, 64)),    # decode kernel, bf16
+             ("q4", 3, 512, (200, 24))]       # decode kernel, Q4
+    calls = []
+    keep = []
+    for fmt, t, n_in, n_outs in cases:
+        b = wl.make_batch(n_in, n_outs, t, fmt, seed=7)
+        weights = [sil.upload_weight(f, buf, n, n_in) for f, buf, n in b.jobs]
+        x = torch.from_numpy(b.x).cuda()
+        ys = [torch.empty((t, n), device="cuda") for n in n_outs]
+        keep.append((weights, x, ys))
+        calls.append((x.data_ptr(), t, n_in, [(w, n, y.data_ptr()) for w, n, y in zip(weights, n_outs, ys)]))
+    stream = torch.cuda.current_stream().cuda_stream
+    for xp, t, n_in, jobs in calls:
+        sil.matmul_batch_noalloc_ptr(xp, t, n_in, jobs, stream)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        for xp, t, n_in, jobs in calls:
+            sil.matmul_batch_noalloc_ptr(xp, t, n_in, jobs, stream)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    sil.check_device_status()
+    for weights, _, _ in keep:
+        for w in weights:
+            w.free()
