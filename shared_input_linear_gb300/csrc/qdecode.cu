@@ -48,6 +48,12 @@ namespace {
 constexpr int kQWarps = 16;
 constexpr int kQThreads = kQWarps * 32;
 constexpr int kMaxQStages = 12;
+// Records per ring stage (consecutive chunks of one tile, one bulk copy): larger
+// copies mean fewer copy operations in flight per SM for the same bytes.
+constexpr int kMaxStageRecords = 4;
+// Relative cost the planner gives each extra CTA a tile's K is split over (the
+// cross-CTA sum through the workspace ends every split tile).
+constexpr double kSplitPenalty = 0.03;
 constexpr int kSlotRounds = 2;          // partial-sum slots per warp row: rounds a warp may run ahead
 constexpr unsigned kStQDecode = 0x10;   // a wait for a record gave up
 constexpr unsigned kStQSlot = 0x20;     // a wait for a free partial-sum slot gave up
@@ -74,6 +80,7 @@ struct QParams {
   int cps;             // chunks per slice
   int wr, wk;          // warp grid: wr row tiles at a time x wk parts of the slice (wr * wk = 16)
   int stages;          // ring stages per warp
+  int spr;             // records per stage: consecutive chunks of one tile, one bulk copy
   int total_tiles;
   int n_jobs;
   int stall;           // failure-detection test: issue no copies, so the waits run out
@@ -96,6 +103,25 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same with a zero accumulator in: d = a * b (the zero register is shared, so
+// no per-call initialisation).
+__device__ __forceinline__ void mma_f16_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Arrival on a per-tile counter in global memory with acquire-release ordering at
+// GPU scope: this thread's earlier writes (and those ordered before it by a warp
+// barrier) are visible before the increment; the last arriver sees every other
+// arriver's writes.  Returns the value before the increment.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* addr, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
 
 __device__ __forceinline__ int find_tile_job(const QParams& p, int tile) {
@@ -116,12 +142,13 @@ __device__ __forceinline__ int x_exponent(unsigned max_bits) {
   return m > 0.f ? max(-126, min(114, ilogbf(m) - 13)) : 0;
 }
 
-// One record: 16 rows x CK columns against the x fragments of that chunk
-// (xb: this lane's fragment of the chunk's first slot, xstep bytes per slot).
+// One record: 16 rows x CK columns against the x fragments of that chunk (xc:
+// this lane's 16 bytes of the chunk's first unit; units 512 bytes apart -- TT = 4:
+// one unit per pair of slots, TT = 8: one per slot).
 // acc: (row g, token col 2q), (row g, col 2q+1), (row g+8, col 2q), (row g+8, col 2q+1).
 template <int FMT, int TT>
-__device__ __forceinline__ void consume_record(const uint8_t* st, int lane, int g, const uint8_t* xb, int xstep,
-                                               bool xvalid, float (&acc)[4]) {
+__device__ __forceinline__ void consume_record(const uint8_t* st, int lane, int g, const uint8_t* xc,
+                                               float (&acc)[4]) {
   using F = QF<FMT>;
   const uint4 q0 = *reinterpret_cast<const uint4*>(st + lane * 16);        // rows 0..7 (group 2p)
   const uint4 q1 = *reinterpret_cast<const uint4*>(st + 512 + lane * 16);  // rows 8..15 (group 2p+1)
@@ -139,18 +166,15 @@ __device__ __forceinline__ void consume_record(const uint8_t* st, int lane, int 
   }
 #pragma unroll
   for (int b = 0; b < F::BLOCKS; ++b) {
-    // B fragments of slots 2b and 2b+1: {high k-pair lo, hi} (and the low parts of x for TT = 8)
-    uint4 xa = make_uint4(0, 0, 0, 0), xc = make_uint4(0, 0, 0, 0);
-    if (xvalid) {
-      if (TT == 8) {
-        xa = *reinterpret_cast<const uint4*>(xb + (2 * b) * xstep);
-        xc = *reinterpret_cast<const uint4*>(xb + (2 * b + 1) * xstep);
-      } else {
-        const uint2 u = *reinterpret_cast<const uint2*>(xb + (2 * b) * xstep);
-        const uint2 v = *reinterpret_cast<const uint2*>(xb + (2 * b + 1) * xstep);
-        xa = make_uint4(u.x, u.y, 0, 0);
-        xc = make_uint4(v.x, v.y, 0, 0);
-      }
+    // B fragments of slots 2b and 2b+1 (TT = 8: high parts in .x/.y, low parts in .z/.w)
+    uint4 xa, xb;
+    if (TT == 8) {
+      xa = *reinterpret_cast<const uint4*>(xc + (2 * b) * 512);
+      xb = *reinterpret_cast<const uint4*>(xc + (2 * b + 1) * 512);
+    } else {
+      const uint4 u = *reinterpret_cast<const uint4*>(xc + b * 512);
+      xa = make_uint4(u.x, u.y, 0u, 0u);
+      xb = make_uint4(u.z, u.w, 0u, 0u);
     }
     uint32_t A0[4], A1[4];  // slots 2b and 2b+1: {row g k-pair lo, row g+8 lo, row g hi, row g+8 hi}
     if (FMT == IL_Q8) {
@@ -168,11 +192,11 @@ __device__ __forceinline__ void consume_record(const uint8_t* st, int lane, int 
       A0[0] = pa[0]; A0[1] = pb[0]; A0[2] = pa[1]; A0[3] = pb[1];
       A1[0] = pa[2]; A1[1] = pb[2]; A1[2] = pa[3]; A1[3] = pb[3];
     }
-    float t4[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_f16(t4, A0, xa.x, xa.y);
+    float t4[4];
+    mma_f16_first(t4, A0, xa.x, xa.y);
     if (TT == 8) mma_f16(t4, A0, xa.z, xa.w);
-    mma_f16(t4, A1, xc.x, xc.y);
-    if (TT == 8) mma_f16(t4, A1, xc.z, xc.w);
+    mma_f16(t4, A1, xb.x, xb.y);
+    if (TT == 8) mma_f16(t4, A1, xb.z, xb.w);
     acc[0] = fmaf(d0[b], t4[0], acc[0]);
     acc[1] = fmaf(d0[b], t4[1], acc[1]);
     acc[2] = fmaf(d1[b], t4[2], acc[2]);
@@ -183,10 +207,9 @@ __device__ __forceinline__ void consume_record(const uint8_t* st, int lane, int 
 // Stores one summed value -- token tk, row `row` of `tile` -- into its job's y.
 // Called by every lane of the warp (the gate/up pairing reads the neighbouring
 // row's sum from the next lane).
-__device__ __forceinline__ void store_item(const QParams& p, int tile, bool have, float v, int row, int tk) {
+__device__ __forceinline__ void store_item(const QParams& p, const QJob& jb, int tile, float v, int row, int tk) {
   const float up = __shfl_down_sync(0xffffffffu, v, 1);  // row + 1 of the same token
-  if (!have || tk >= p.t) return;
-  const QJob& jb = p.jobs[find_tile_job(p, tile)];
+  if (tk >= p.t) return;
   const int r = (tile - jb.tile_begin) * 16 + row;
   if (r >= jb.n_out) return;
   if (jb.glu) {
@@ -224,11 +247,12 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
   const int rounds = stream < tg_total ? (tg_total - stream + nstreams - 1) / nstreams : 0;
 
   // shared memory: x fragments | rings | partial sums | slot counts | barriers
-  const int xslot = 64 * p.t;  // bytes per 16-column slot of x fragments
-  const size_t xs_bytes = ((size_t)p.cps * F::SLOTS * xslot + 127) & ~(size_t)127;
+  constexpr int XCHUNK = F::SLOTS * 32 * XL;  // bytes of x fragments per chunk
+  const size_t xs_bytes = (size_t)p.cps * XCHUNK;
   uint8_t* xs = smem;
-  uint8_t* ring = smem + xs_bytes + (size_t)warp * D * RS;
-  float* part = reinterpret_cast<float*>(smem + xs_bytes + (size_t)kQWarps * D * RS);  // [NB][16 warps][TT][16]
+  const int SB_ = p.spr * RS;  // bytes per ring stage
+  uint8_t* ring = smem + xs_bytes + (size_t)warp * D * SB_;
+  float* part = reinterpret_cast<float*>(smem + xs_bytes + (size_t)kQWarps * D * SB_);  // [NB][16 warps][TT][16]
   int* cnt_s = reinterpret_cast<int*>(part + kSlotRounds * kQWarps * TT * 16);           // [NB][16 rows of warps]
   int* gen_s = cnt_s + kSlotRounds * kQWarps;                                            // [NB][16]
   uint64_t* bars = reinterpret_cast<uint64_t*>(gen_s + kSlotRounds * kQWarps) + warp * kMaxQStages;
@@ -263,12 +287,15 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
   if (lane == 0 && cnt > 0) l_src = tile_records(0);
   auto issue_next = [&]() {
     if (l_src == nullptr) return;
+    const int nr = min(p.spr, cnt - l_cc);
     const uint32_t bar = smem_u32(&bars[l_stage]);
-    mbar_expect_tx(bar, RS);
-    if (!p.stall) bulk_g2s_hint(smem_u32(ring + (size_t)l_stage * RS), l_src + (size_t)l_cc * RS, RS, bar, policy);
+    mbar_expect_tx(bar, nr * RS);
+    if (!p.stall)
+      bulk_g2s_hint(smem_u32(ring + (size_t)l_stage * SB_), l_src + (size_t)l_cc * RS, nr * RS, bar, policy);
     ++issued;
     if (++l_stage == D) l_stage = 0;
-    if (++l_cc == cnt) {
+    l_cc += nr;
+    if (l_cc == cnt) {
       l_cc = 0;
       l_src = tile_records(++l_round);
     }
@@ -281,51 +308,86 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
   grid_dep_launch();
 
   // ---- x of this CTA's slice as B fragments, token by token scaled by 2^-e(tok)
-  // so that its largest |x| in the slice lies in [2^13, 2^14).  Fragment layout:
-  // [slot][compact lane] -- TT = 8: lanes 4 tok + q hold {high, low} parts (16 bytes);
-  // TT = 4: lanes 8 tok + 4 h + q hold the high (h = 0) or low (h = 1) part (8 bytes).
-  const int cols = ns * F::CK;
+  // so that its largest |x| in the slice lies in [2^13, 2^14).  Per chunk, units
+  // of 512 bytes, lane L's 16 bytes at 16 L: TT = 8, one unit per slot, {high,
+  // low} parts of token L/4; TT = 4, one unit per pair of slots, the high part
+  // (L/4 < 4) or low part (L/4 >= 4) of token (L/4) % 4 for both slots.  Lanes of
+  // tokens >= t hold zeros.
+  // (loads are issued 8 at a time before they are used: x comes from L2, and a
+  // chain of dependent loads would hold every warp up before the first record)
+  const int c4n = ns * F::CK / 4;
   for (int tk = 0; tk < p.t; ++tk) {
     const float* xrow = p.x + (size_t)tk * p.x_row_stride + (size_t)cb * F::CK;
+    const int c4max = min(c4n, (p.n_in - cb * F::CK) / 4);  // float4s inside n_in
     float mx = 0.f;
-    for (int c4 = threadIdx.x; c4 < cols / 4; c4 += kQThreads)
-      if (cb * F::CK + 4 * c4 < p.n_in) {
-        const float4 v = *reinterpret_cast<const float4*>(xrow + 4 * c4);
-        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-      }
+    for (int c4 = threadIdx.x; c4 < c4max; c4 += 8 * kQThreads) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = c4 + u * kQThreads < c4max ? __ldg(reinterpret_cast<const float4*>(xrow) + c4 + u * kQThreads)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w))));
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0 && mx > 0.f) atomicMax(&tok_max[tk], __float_as_uint(mx));  // non-negative: bits order as values
   }
   __syncthreads();
-  const int lanes_per_slot = (TT == 8 ? 4 : 8) * p.t;
-  for (int e = threadIdx.x; e < ns * F::SLOTS * lanes_per_slot; e += kQThreads) {
-    const int sl = e / lanes_per_slot, ci = e - (e / lanes_per_slot) * lanes_per_slot;
-    const int tk = TT == 8 ? ci >> 2 : ci >> 3;
-    const int qq = ci & 3;
-    const int col = cb * F::CK + (sl / F::SLOTS) * F::CK + 16 * (sl % F::SLOTS) + 4 * qq;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (col < p.n_in) v = *reinterpret_cast<const float4*>(p.x + (size_t)tk * p.x_row_stride + col);
-    const float xsc = ldexpf(1.0f, -x_exponent(tok_max[tk]));
-    const __half2 h01 = __floats2half2_rn(v.x * xsc, v.y * xsc);
-    const __half2 h23 = __floats2half2_rn(v.z * xsc, v.w * xsc);
-    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-    const __half2 l01 = __floats2half2_rn(v.x * xsc - f01.x, v.y * xsc - f01.y);
-    const __half2 l23 = __floats2half2_rn(v.z * xsc - f23.x, v.w * xsc - f23.y);
-    uint8_t* dst = xs + (size_t)sl * xslot + ci * XL;
-    if (TT == 8) {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(h2_bits(h01), h2_bits(h23), h2_bits(l01), h2_bits(l23));
-    } else {
-      const bool low = (ci >> 2) & 1;
-      *reinterpret_cast<uint2*>(dst) = low ? make_uint2(h2_bits(l01), h2_bits(l23)) : make_uint2(h2_bits(h01), h2_bits(h23));
+  constexpr int kSlotsPerUnit = TT == 8 ? 1 : 2;
+  constexpr int kUnroll = 4;
+  const int n_el = ns * (F::SLOTS / kSlotsPerUnit) * 32;
+  for (int e0 = threadIdx.x; e0 < n_el; e0 += kUnroll * kQThreads) {
+    float4 v[kUnroll][kSlotsPerUnit];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int e = e0 + u * kQThreads;
+      const int L = e & 31, unit = e >> 5;
+      const int tk = TT == 8 ? (L >> 2) : ((L >> 2) & 3);
+#pragma unroll
+      for (int h = 0; h < kSlotsPerUnit; ++h) {
+        const int col = cb * F::CK + 16 * (unit * kSlotsPerUnit + h) + 4 * (L & 3);
+        v[u][h] = (e < n_el && tk < p.t && col < p.n_in)
+                      ? __ldg(reinterpret_cast<const float4*>(p.x + (size_t)tk * p.x_row_stride + col))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int e = e0 + u * kQThreads;
+      if (e >= n_el) break;
+      const int L = e & 31, unit = e >> 5;
+      const int gg = L >> 2;
+      const int tk = TT == 8 ? gg : (gg & 3);
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      if (tk < p.t) {
+        const float xsc = ldexpf(1.0f, -x_exponent(tok_max[tk]));
+#pragma unroll
+        for (int h = 0; h < kSlotsPerUnit; ++h) {
+          const float4 x4 = v[u][h];
+          const __half2 h01 = __floats2half2_rn(x4.x * xsc, x4.y * xsc);
+          const __half2 h23 = __floats2half2_rn(x4.z * xsc, x4.w * xsc);
+          const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+          const __half2 l01 = __floats2half2_rn(x4.x * xsc - f01.x, x4.y * xsc - f01.y);
+          const __half2 l23 = __floats2half2_rn(x4.z * xsc - f23.x, x4.w * xsc - f23.y);
+          if (TT == 8) {
+            w[0] = h2_bits(h01);
+            w[1] = h2_bits(h23);
+            w[2] = h2_bits(l01);
+            w[3] = h2_bits(l23);
+          } else {
+            const bool low = gg >= 4;
+            w[2 * h] = low ? h2_bits(l01) : h2_bits(h01);
+            w[2 * h + 1] = low ? h2_bits(l23) : h2_bits(h23);
+          }
+        }
+      }
+      *reinterpret_cast<uint4*>(xs + (size_t)unit * 512 + L * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
   __syncthreads();
-  // this lane's B fragment: column g is token g (TT = 8) or the high / low part of token g % 4
-  const int my_tok = TT == 8 ? g : (g & 3);
-  const bool xvalid = my_tok < p.t;
-  const int my_ci = TT == 8 ? 4 * g + q : 8 * (g & 3) + 4 * (g >> 2) + q;
-  const uint8_t* xlane = xs + my_ci * XL;
+  const uint8_t* xlane = xs + lane * 16;
   // scale back of the partials: this lane's D columns are tokens 2q and 2q+1
   // (for t <= 4, lanes q < 2 after folding the low-part columns in)
   const int tq0 = TT == 8 ? 2 * q : 2 * (q & 1), tq1 = tq0 + 1;
@@ -336,16 +398,26 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
   uint32_t c_phase = 0;
   int consumed = 0;
   bool ok = true;
+  auto wait_stage = [&](int st_i, uint32_t ph) {
+    return __all_sync(0xffffffffu, mbar_wait_sleep(smem_u32(&bars[st_i]), ph, abort_flag, p.status, kStQDecode));
+  };
   for (int r = 0; r < rounds; ++r) {
     const int tile = (stream + r * nstreams) * p.wr + wr_i;
     if (tile >= p.total_tiles) break;  // same for the whole row of warps, and for every later round
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int cc = 0; cc < cnt && ok; ++cc) {
-      const uint32_t bar = smem_u32(&bars[c_stage]);
-      ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar, c_phase, abort_flag, p.status, kStQDecode));
+    const uint8_t* xcc = xlane + (size_t)c0 * XCHUNK;
+    // one stage at a time: up to spr consecutive chunks of this tile, one wait and
+    // one refill for all of them
+    for (int cc = 0; cc < cnt && ok; cc += p.spr) {
+      const int nr = min(p.spr, cnt - cc);
+      ok = wait_stage(c_stage, c_phase);
       if (!ok) break;
-      consume_record<FMT, TT>(ring + (size_t)c_stage * RS, lane, g, xlane + (size_t)(c0 + cc) * F::SLOTS * xslot,
-                              xslot, xvalid, acc);
+      const uint8_t* st = ring + (size_t)c_stage * SB_;
+      consume_record<FMT, TT>(st, lane, g, xcc, acc);
+#pragma unroll
+      for (int i = 1; i < kMaxStageRecords; ++i)
+        if (i < nr) consume_record<FMT, TT>(st + i * RS, lane, g, xcc + i * XCHUNK, acc);
+      xcc += (size_t)nr * XCHUNK;
       ++consumed;
       // every lane's reads of this stage are done before the copy that refills it
       __syncwarp();
@@ -387,15 +459,18 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
       pw[(2 * q + 1) * 16 + g + 8] = acc[3] * ys1;
     }
     __syncwarp();
-    int last = 0;
-    if (lane == 0) {
+    int last = 1;
+    if (p.wk > 1) {
+      if (lane == 0) {
+        __threadfence_block();
+        last = atomicAdd(&cnt_s[slot], 1) == p.wk - 1;
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) continue;
       __threadfence_block();
-      last = atomicAdd(&cnt_s[slot], 1) == p.wk - 1;
     }
-    if (!__shfl_sync(0xffffffffu, last, 0)) continue;
     // ---- the last of the tile's wk parts: sum them in part order, (token, row)
     // items with rows fastest
-    __threadfence_block();
     const float* pr = part + (size_t)((sr * kQWarps + wr_i * p.wk) * TT) * 16;
     float v[NI];
 #pragma unroll
@@ -409,22 +484,21 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
     }
     __syncwarp();
     if (lane == 0) {
-      cnt_s[slot] = 0;
+      if (p.wk > 1) cnt_s[slot] = 0;
       __threadfence_block();
       atomicAdd(&gen_s[slot], 1);  // the slot may be written again
     }
     if (p.slices > 1) {
       // ---- then over the C slices, through the global workspace: the last CTA to
-      // arrive adds them in slice order
+      // arrive adds them in slice order (one thread fences for the warp, around the
+      // warp-wide stores and loads)
       float* wsp = p.ws + ((size_t)tile * p.slices + rank) * TT * 16;
 #pragma unroll
       for (int i = 0; i < NI; ++i) __stcg(wsp + lane + 32 * i, v[i]);
-      __threadfence();
       __syncwarp();
       int lastc = 0;
-      if (lane == 0) lastc = atomicAdd(p.counters + tile, 1u) == (unsigned)(p.slices - 1);
+      if (lane == 0) lastc = atom_add_acq_rel_gpu(p.counters + tile, 1u) == (unsigned)(p.slices - 1);
       if (!__shfl_sync(0xffffffffu, lastc, 0)) continue;
-      __threadfence();
       const float* wt = p.ws + (size_t)tile * p.slices * TT * 16;
 #pragma unroll
       for (int i = 0; i < NI; ++i) {
@@ -434,10 +508,11 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
       }
       if (lane == 0) p.counters[tile] = 0u;  // zero again for the next launch
     }
+    const QJob& jb = p.jobs[find_tile_job(p, tile)];
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
       const int e = lane + 32 * i;
-      store_item(p, tile, true, v[i], e & 15, e >> 4);
+      store_item(p, jb, tile, v[i], e & 15, e >> 4);
     }
   }
   // after a wait gave up: let the copies this warp still has in flight land
@@ -467,7 +542,7 @@ QKernelFn select_q(int fmt, int TT) {
 }
 
 size_t q_x_bytes(int fmt, int t, int cps) {
-  return ((size_t)cps * (chunk_k(fmt) / 16) * 64 * t + 127) & ~(size_t)127;
+  return (size_t)cps * (chunk_k(fmt) / 16) * 32 * (t <= 4 ? 8 : 16);
 }
 
 // Shared memory besides the x fragments and the rings.
@@ -495,7 +570,7 @@ int q_smem_limit(int dev) {
 }
 
 struct QPlan {
-  int C = 0, cps = 0, wr = 0, wk = 0, stages = 0, streams = 0;
+  int C = 0, cps = 0, wr = 0, wk = 0, stages = 0, spr = 1, streams = 0;
   size_t smem = 0, ws_bytes = 0;
 };
 
@@ -520,29 +595,36 @@ bool plan_q(int fmt, int t, int n_chunks, int total_tiles, int num_sms, int smem
     }
     const size_t fixed = q_x_bytes(fmt, t, cps) + q_fixed_bytes(TT);
     if (fixed >= (size_t)smem_limit) continue;
-    int stages = (int)(((size_t)smem_limit - fixed) / ((size_t)kQWarps * record_bytes(fmt)));
-    if (stages > kMaxQStages) stages = kMaxQStages;
-    if (stages < 3) continue;
     const int streams = num_sms / c;
-    for (int wk = kQWarps; wk >= 1; wk /= 2) {
-      const int wr = kQWarps / wk;
-      const int cpw = (cps + wk - 1) / wk;
-      const int tg = (total_tiles + wr - 1) / wr;
-      const int used = tg < streams ? tg : streams;
-      const int rounds = (tg + used - 1) / used;
-      const double eff = work / ((double)num_sms * rounds * wr * cps);
-      const int busy = (cps < wk ? cps : wk) * wr;  // warps with records in a full round
-      const double score = eff * (1.0 - 0.03 * (c - 1)) * (busy >= 8 ? 1.0 : busy / 8.0) * cpw / (cpw + 0.5);
-      if (score > best) {
-        best = score;
-        out->C = c;
-        out->cps = cps;
-        out->wr = wr;
-        out->wk = wk;
-        out->stages = stages;
-        out->streams = used;
-        out->smem = fixed + (size_t)kQWarps * stages * record_bytes(fmt);
-        out->ws_bytes = ws;
+    for (int spr = kMaxStageRecords; spr >= 1; spr /= 2) {
+      int stages = (int)(((size_t)smem_limit - fixed) / ((size_t)kQWarps * spr * record_bytes(fmt)));
+      if (stages > kMaxQStages) stages = kMaxQStages;
+      if (stages < 2) continue;
+      for (int wk = kQWarps; wk >= 1; wk /= 2) {
+        const int wr = kQWarps / wk;
+        const int cpw = (cps + wk - 1) / wk;
+        const int tg = (total_tiles + wr - 1) / wr;
+        const int used = tg < streams ? tg : streams;
+        const int rounds = (tg + used - 1) / used;
+        const double eff = work / ((double)num_sms * rounds * wr * cps);
+        const int busy = (cps < wk ? cps : wk) * wr;  // warps with records in a full round
+        // measured: copies of one record stream at about 0.7 of four-record copies
+        const int per_copy = cpw < spr ? cpw : spr;
+        const double copy = per_copy >= 4 ? 1.0 : (per_copy == 3 ? 0.96 : (per_copy == 2 ? 0.88 : 0.72));
+        const double score = eff * (1.0 - kSplitPenalty * (c - 1)) * (busy >= 8 ? 1.0 : busy / 8.0) *
+                             cpw / (cpw + 0.5) * copy;
+        if (score > best) {
+          best = score;
+          out->C = c;
+          out->cps = cps;
+          out->wr = wr;
+          out->wk = wk;
+          out->stages = stages;
+          out->spr = spr;
+          out->streams = used;
+          out->smem = fixed + (size_t)kQWarps * stages * spr * record_bytes(fmt);
+          out->ws_bytes = ws;
+        }
       }
     }
   }
@@ -591,6 +673,7 @@ cudaError_t prepare_qdecode(int fmt, const DecodeParams& d, int num_sms, unsigne
   p.wr = pl.wr;
   p.wk = pl.wk;
   p.stages = pl.stages;
+  p.spr = pl.spr;
   p.total_tiles = d.total_groups / 2;
   p.n_jobs = d.n_jobs;
   for (int j = 0; j < d.n_jobs; ++j) {
