@@ -258,7 +258,8 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
   uint64_t* bars = reinterpret_cast<uint64_t*>(gen_s + kSlotRounds * kQWarps) + warp * kMaxQStages;
   unsigned* tok_max = reinterpret_cast<unsigned*>(reinterpret_cast<uint64_t*>(gen_s + kSlotRounds * kQWarps) +
                                                   kQWarps * kMaxQStages);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tok_max + 8);
+  float* tok_scale = reinterpret_cast<float*>(tok_max + 8);  // 2^-e(tok): x into fp16 range
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tok_scale + 8);
 
   if (lane == 0)
     for (int s = 0; s < D; ++s) mbar_init(smem_u32(&bars[s]), 1);
@@ -316,24 +317,33 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
   // (loads are issued 8 at a time before they are used: x comes from L2, and a
   // chain of dependent loads would hold every warp up before the first record)
   const int c4n = ns * F::CK / 4;
-  for (int tk = 0; tk < p.t; ++tk) {
-    const float* xrow = p.x + (size_t)tk * p.x_row_stride + (size_t)cb * F::CK;
+  {
     const int c4max = min(c4n, (p.n_in - cb * F::CK) / 4);  // float4s inside n_in
-    float mx = 0.f;
-    for (int c4 = threadIdx.x; c4 < c4max; c4 += 8 * kQThreads) {
-      float4 v[8];
+    const float4* xr4 = reinterpret_cast<const float4*>(p.x + (size_t)cb * F::CK);
+    float mx[TT];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        v[u] = c4 + u * kQThreads < c4max ? __ldg(reinterpret_cast<const float4*>(xrow) + c4 + u * kQThreads)
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int tk = 0; tk < TT; ++tk) mx[tk] = 0.f;
+    // every token's float4 of a column block in flight at once
+#pragma unroll 2
+    for (int c4 = threadIdx.x; c4 < c4max; c4 += kQThreads) {
+      float4 v[TT];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w))));
+      for (int tk = 0; tk < TT; ++tk)
+        v[tk] = tk < p.t ? __ldg(xr4 + (size_t)tk * (p.x_row_stride / 4) + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int tk = 0; tk < TT; ++tk)
+        mx[tk] = fmaxf(mx[tk], fmaxf(fmaxf(fabsf(v[tk].x), fabsf(v[tk].y)), fmaxf(fabsf(v[tk].z), fabsf(v[tk].w))));
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0 && mx > 0.f) atomicMax(&tok_max[tk], __float_as_uint(mx));  // non-negative: bits order as values
+    for (int tk = 0; tk < TT; ++tk) {
+      float m = mx[tk];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0 && m > 0.f) atomicMax(&tok_max[tk], __float_as_uint(m));  // non-negative: bits order as values
+    }
   }
+  __syncthreads();
+  if (threadIdx.x < 8) tok_scale[threadIdx.x] = ldexpf(1.0f, -x_exponent(tok_max[threadIdx.x]));
   __syncthreads();
   constexpr int kSlotsPerUnit = TT == 8 ? 1 : 2;
   constexpr int kUnroll = 4;
@@ -362,7 +372,7 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
       const int tk = TT == 8 ? gg : (gg & 3);
       uint32_t w[4] = {0u, 0u, 0u, 0u};
       if (tk < p.t) {
-        const float xsc = ldexpf(1.0f, -x_exponent(tok_max[tk]));
+        const float xsc = tok_scale[tk];
 #pragma unroll
         for (int h = 0; h < kSlotsPerUnit; ++h) {
           const float4 x4 = v[u][h];
@@ -548,7 +558,7 @@ size_t q_x_bytes(int fmt, int t, int cps) {
 // Shared memory besides the x fragments and the rings.
 size_t q_fixed_bytes(int TT) {
   return (size_t)kSlotRounds * kQWarps * TT * 16 * sizeof(float) + 2 * (size_t)kSlotRounds * kQWarps * sizeof(int) +
-         (size_t)kQWarps * kMaxQStages * 8 + 8 * sizeof(unsigned) + 16;
+         (size_t)kQWarps * kMaxQStages * 8 + 8 * sizeof(unsigned) + 8 * sizeof(float) + 16;
 }
 
 // Dynamic shared memory a CTA may take, once per device (the kernels' attribute
@@ -584,7 +594,13 @@ bool plan_q(int fmt, int t, int n_chunks, int total_tiles, int num_sms, int smem
   const int TT = t <= 4 ? 4 : 8;
   const double work = (double)total_tiles * n_chunks;
   double best = -1.0;
+  // with tiles for many rounds on every SM, a K split evens nothing out and only
+  // adds the cross-CTA sum to every tile: keep C = 1 whenever its x fits
+  const bool many_tiles = total_tiles >= 4 * num_sms * kQWarps;
+  const bool unsplit_fits = q_x_bytes(fmt, t, n_chunks) + q_fixed_bytes(TT) +
+                                2 * (size_t)kQWarps * record_bytes(fmt) <= (size_t)smem_limit;
   for (int c = 1; c <= 8 && c <= n_chunks; ++c) {
+    if (c > 1 && many_tiles && unsplit_fits) break;
     const int cps = (n_chunks + c - 1) / c;
     if ((n_chunks + cps - 1) / cps != c) continue;
     size_t ws = 0;
