@@ -16,11 +16,11 @@
 //  * Dot products run on the tensor cores (mma.m16n8k16, fp16 in, fp32
 //    accumulate).  The 16 weight rows of a record are the A operand, decoded in
 //    registers to exact fp16 integers (one byte permute or LOP3 and one fp16x2
-//    subtract per pair); x is the B operand, its tokens the 8 columns, split into
-//    an fp16 high part and the fp16 rounding of the remainder (about 22
-//    significant bits): side by side in the columns for t <= 4 (one MMA per 16
-//    columns of K), as two chained MMAs for t <= 8.  The fp32 scale of each
-//    32-block multiplies the fp32 partial of that block.
+//    subtract per pair); x is the B operand, its tokens the 8 columns: for t <= 4
+//    an fp16 high part and the fp16 rounding of the remainder side by side (about
+//    22 significant bits), for t <= 8 the fp16 value (11 bits); one MMA per 16
+//    columns of K either way.  The fp32 scale of each 32-block multiplies the
+//    fp32 partial of that block.
 //  * x is staged once per CTA in shared memory, already as B fragments, only for
 //    the lanes whose token exists (4 t bytes per column), scaled per token by a
 //    power of two so that fp16 holds it (undone on the partial sums).
@@ -143,8 +143,8 @@ __device__ __forceinline__ int x_exponent(unsigned max_bits) {
 }
 
 // One record: 16 rows x CK columns against the x fragments of that chunk (xc:
-// this lane's 16 bytes of the chunk's first unit; units 512 bytes apart -- TT = 4:
-// one unit per pair of slots, TT = 8: one per slot).
+// this lane's 16 bytes of the chunk's first unit; one unit of 512 bytes per pair
+// of slots).
 // acc: (row g, token col 2q), (row g, col 2q+1), (row g+8, col 2q), (row g+8, col 2q+1).
 template <int FMT, int TT>
 __device__ __forceinline__ void consume_record(const uint8_t* st, int lane, int g, const uint8_t* xc,
@@ -166,16 +166,8 @@ __device__ __forceinline__ void consume_record(const uint8_t* st, int lane, int 
   }
 #pragma unroll
   for (int b = 0; b < F::BLOCKS; ++b) {
-    // B fragments of slots 2b and 2b+1 (TT = 8: high parts in .x/.y, low parts in .z/.w)
-    uint4 xa, xb;
-    if (TT == 8) {
-      xa = *reinterpret_cast<const uint4*>(xc + (2 * b) * 512);
-      xb = *reinterpret_cast<const uint4*>(xc + (2 * b + 1) * 512);
-    } else {
-      const uint4 u = *reinterpret_cast<const uint4*>(xc + b * 512);
-      xa = make_uint4(u.x, u.y, 0u, 0u);
-      xb = make_uint4(u.z, u.w, 0u, 0u);
-    }
+    // B fragments of slots 2b and 2b+1: one 16-byte load, one MMA per slot
+    const uint4 u = *reinterpret_cast<const uint4*>(xc + b * 512);
     uint32_t A0[4], A1[4];  // slots 2b and 2b+1: {row g k-pair lo, row g+8 lo, row g hi, row g+8 hi}
     if (FMT == IL_Q8) {
       uint32_t p01, p23, r01, r23;
@@ -193,10 +185,8 @@ __device__ __forceinline__ void consume_record(const uint8_t* st, int lane, int 
       A1[0] = pa[2]; A1[1] = pb[2]; A1[2] = pa[3]; A1[3] = pb[3];
     }
     float t4[4];
-    mma_f16_first(t4, A0, xa.x, xa.y);
-    if (TT == 8) mma_f16(t4, A0, xa.z, xa.w);
-    mma_f16(t4, A1, xb.x, xb.y);
-    if (TT == 8) mma_f16(t4, A1, xb.z, xb.w);
+    mma_f16_first(t4, A0, u.x, u.y);
+    mma_f16(t4, A1, u.z, u.w);
     acc[0] = fmaf(d0[b], t4[0], acc[0]);
     acc[1] = fmaf(d0[b], t4[1], acc[1]);
     acc[2] = fmaf(d1[b], t4[2], acc[2]);
@@ -224,7 +214,7 @@ template <int FMT, int TT>
 __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_constant__ QParams p) {
   using F = QF<FMT>;
   constexpr int RS = F::RS;
-  constexpr int XL = TT == 8 ? 16 : 8;  // bytes of one lane's B fragment per slot
+  constexpr int XL = 8;                 // bytes of one lane's B fragment per slot
   constexpr int NI = TT / 2;            // summed items per lane: TT tokens x 16 rows over 32 lanes
   extern __shared__ __align__(128) uint8_t smem[];
 
@@ -309,11 +299,11 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
   grid_dep_launch();
 
   // ---- x of this CTA's slice as B fragments, token by token scaled by 2^-e(tok)
-  // so that its largest |x| in the slice lies in [2^13, 2^14).  Per chunk, units
-  // of 512 bytes, lane L's 16 bytes at 16 L: TT = 8, one unit per slot, {high,
-  // low} parts of token L/4; TT = 4, one unit per pair of slots, the high part
-  // (L/4 < 4) or low part (L/4 >= 4) of token (L/4) % 4 for both slots.  Lanes of
-  // tokens >= t hold zeros.
+  // so that its largest |x| in the slice lies in [2^13, 2^14).  Per chunk, one
+  // unit of 512 bytes per pair of slots, lane L's 16 bytes at 16 L holding its B
+  // fragment of both slots: TT = 8, the fp16 of token L/4; TT = 4, the fp16 high
+  // part (L/4 < 4) or the fp16 rounding of the remainder (L/4 >= 4) of token
+  // (L/4) % 4.  Lanes of tokens >= t hold zeros.
   // (loads are issued 8 at a time before they are used: x comes from L2, and a
   // chain of dependent loads would hold every warp up before the first record)
   const int c4n = ns * F::CK / 4;
@@ -345,7 +335,7 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
   __syncthreads();
   if (threadIdx.x < 8) tok_scale[threadIdx.x] = ldexpf(1.0f, -x_exponent(tok_max[threadIdx.x]));
   __syncthreads();
-  constexpr int kSlotsPerUnit = TT == 8 ? 1 : 2;
+  constexpr int kSlotsPerUnit = 2;
   constexpr int kUnroll = 4;
   const int n_el = ns * (F::SLOTS / kSlotsPerUnit) * 32;
   for (int e0 = threadIdx.x; e0 < n_el; e0 += kUnroll * kQThreads) {
@@ -381,16 +371,9 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
           const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
           const __half2 l01 = __floats2half2_rn(x4.x * xsc - f01.x, x4.y * xsc - f01.y);
           const __half2 l23 = __floats2half2_rn(x4.z * xsc - f23.x, x4.w * xsc - f23.y);
-          if (TT == 8) {
-            w[0] = h2_bits(h01);
-            w[1] = h2_bits(h23);
-            w[2] = h2_bits(l01);
-            w[3] = h2_bits(l23);
-          } else {
-            const bool low = gg >= 4;
-            w[2 * h] = low ? h2_bits(l01) : h2_bits(h01);
-            w[2 * h + 1] = low ? h2_bits(l23) : h2_bits(h23);
-          }
+          const bool low = TT == 4 && gg >= 4;
+          w[2 * h] = low ? h2_bits(l01) : h2_bits(h01);
+          w[2 * h + 1] = low ? h2_bits(l23) : h2_bits(h23);
         }
       }
       *reinterpret_cast<uint4*>(xs + (size_t)unit * 512 + L * 16) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -552,7 +535,8 @@ QKernelFn select_q(int fmt, int TT) {
 }
 
 size_t q_x_bytes(int fmt, int t, int cps) {
-  return (size_t)cps * (chunk_k(fmt) / 16) * 32 * (t <= 4 ? 8 : 16);
+  (void)t;
+  return (size_t)cps * (chunk_k(fmt) / 16) * 32 * 8;
 }
 
 // Shared memory besides the x fragments and the rings.
