@@ -156,27 +156,59 @@ constexpr unsigned kStMma = 0x2;
 constexpr unsigned kStEpilogue = 0x4;
 constexpr unsigned kStTransform = 0x8;
 
+// Two fp32 values as one 64-bit register pair, and the packed fp32 operations
+// of sm_100-class cores on them (one instruction for both lanes).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// bf16x2 (round to nearest even) of a pair.
+__device__ __forceinline__ uint32_t f2bf16x2(uint64_t v) {
+  float lo, hi;
+  f2unpack(v, lo, hi);
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Dequantise one 16-byte unit of an A tile (row r, columns 8u .. 8u+7 of the
 // k-block) from a raw stage: 8 consecutive columns of one row sit in two
 // neighbouring lanes' words of the packed chunk (4 columns each) and share one
-// 32-block scale.  half: which 64 columns of a Q4 chunk (128 columns) this k-block is.
+// 32-block scale.  half: which 64 columns of a Q4 chunk (128 columns) this k-block
+// is.  Each value is bf16(fp32(d * q)): q exact in fp32, one rounded multiply,
+// one round to bf16.  Q8: a byte permute puts the stored byte u = q + 128 under
+// the exponent of 2^23 (the float 2^23 + u) and one packed subtract leaves q;
+// Q4: the nibbles decode to exact fp16 and widen.
 template <int FMT>
 __device__ __forceinline__ uint4 dequant_unit(const uint32_t* __restrict__ qw, const float* __restrict__ sc, int r,
                                               int u, int half) {
   const int gl = r >> 3, n = r & 7;
   const int q0 = (u & 1) * 2;
-  float q[8];
+  uint64_t qp[4];  // four pairs of q as fp32
   float d;
   if (FMT == IL_Q8) {
     const int base = gl * 128 + (4 * n + q0) * 4 + (u >> 1);
+    const uint64_t bias = f2pack(8388736.0f, 8388736.0f);  // 2^23 + 128
 #pragma unroll
     for (int h = 0; h < 2; ++h) {  // lanes q0 and q0 + 1
-      uint32_t p01, p23;
-      q8_word_to_f16x2(qw[base + 4 * h], p01, p23);
-      q[4 * h] = f16_lo(p01);
-      q[4 * h + 1] = f16_hi(p01);
-      q[4 * h + 2] = f16_lo(p23);
-      q[4 * h + 3] = f16_hi(p23);
+      const uint32_t w = qw[base + 4 * h];
+      qp[2 * h] = f2sub(f2pack(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540)),
+                               __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7541))), bias);
+      qp[2 * h + 1] = f2sub(f2pack(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7542)),
+                                   __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7543))), bias);
     }
     d = sc[gl * 16 + n * 2 + (u >> 2)];
   } else {
@@ -187,20 +219,16 @@ __device__ __forceinline__ uint4 dequant_unit(const uint32_t* __restrict__ qw, c
       uint32_t prs[4];
       q4_word_to_f16x2(qw[base + 4 * h], prs);
       const uint32_t p01 = sub ? prs[2] : prs[0], p23 = sub ? prs[3] : prs[1];  // no local-memory indexing
-      q[4 * h] = f16_lo(p01);
-      q[4 * h + 1] = f16_hi(p01);
-      q[4 * h + 2] = f16_lo(p23);
-      q[4 * h + 3] = f16_hi(p23);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&p01));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&p23));
+      qp[2 * h] = f2pack(a.x, a.y);
+      qp[2 * h + 1] = f2pack(b.x, b.y);
     }
     d = sc[gl * 32 + n * 4 + w];
   }
-  uint32_t o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(d, q[2 * i]), __fmul_rn(d, q[2 * i + 1]));
-    o[i] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
+  const uint64_t dd = f2pack(d, d);
+  return make_uint4(f2bf16x2(f2mul(dd, qp[0])), f2bf16x2(f2mul(dd, qp[1])), f2bf16x2(f2mul(dd, qp[2])),
+                    f2bf16x2(f2mul(dd, qp[3])));
 }
 
 template <int BN, int FMT>
