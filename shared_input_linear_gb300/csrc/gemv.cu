@@ -38,6 +38,7 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSliceK = 4096;  // columns of x staged per CTA (32 bytes each)
+constexpr int kStageUnroll = 4;   // x loads in flight per thread while staging
 
 // Not volatile: independent MMAs (different accumulators) may be interleaved by
 // the scheduler, which hides the tensor-pipe latency of each accumulate chain.
@@ -134,18 +135,39 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
   // the next kernel may now be scheduled; it waits for this one before touching x or y
   grid_dep_launch();
 
-  // ---- stage this CTA's K slice of x in fragment order (hi/lo split)
-  for (int e = threadIdx.x; e < slots * 32; e += kThreads) {
-    const int sl = e >> 5, L = e & 31, qq = L & 3;
-    const int m = L >> 2;
-    const int k = kChunkK * (c_begin + (sl >> 1)) + 8 * qq + 4 * (sl & 1);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (m < p.t && k < p.n_in && sl < c_cnt * kSlotsPerChunk) {
-      const float4 xv = *reinterpret_cast<const float4*>(p.x + (int64_t)m * p.x_row_stride + k);
-      split_pair(xv.x, xv.y, v.x, v.y);
-      split_pair(xv.z, xv.w, v.z, v.w);
+  // ---- stage this CTA's K slice of x in fragment order (hi/lo split).  Lane L
+  // of a slot holds token L/4: the fragments of tokens >= t are zeros, and the
+  // float4 loads of the others are spread over all threads and issued
+  // kStageUnroll at a time (x comes from L2: a chain of dependent loads would
+  // hold the CTA back by one L2 round trip per iteration).
+  for (int e = threadIdx.x; e < slots * 32; e += kThreads)
+    if (((e & 31) >> 2) >= p.t) xf[e] = make_uint4(0, 0, 0, 0);
+  const int per_slot = 4 * p.t;  // fragments with data per slot: lanes 0 .. 4t-1
+  const int n_src = slots * per_slot;
+  for (int e0 = threadIdx.x; e0 < n_src; e0 += kStageUnroll * kThreads) {
+    float4 xv[kStageUnroll];
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u) {
+      const int e = e0 + u * kThreads;
+      xv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < n_src) {
+        const int sl = e / per_slot, L = e - sl * per_slot;
+        const int k = kChunkK * (c_begin + (sl >> 1)) + 8 * (L & 3) + 4 * (sl & 1);
+        if (k < p.n_in && sl < c_cnt * kSlotsPerChunk)
+          xv[u] = *reinterpret_cast<const float4*>(p.x + (int64_t)(L >> 2) * p.x_row_stride + k);
+      }
     }
-    xf[e] = v;
+#pragma unroll
+    for (int u = 0; u < kStageUnroll; ++u) {
+      const int e = e0 + u * kThreads;
+      if (e < n_src) {
+        const int sl = e / per_slot, L = e - sl * per_slot;
+        uint4 v;
+        split_pair(xv[u].x, xv[u].y, v.x, v.y);
+        split_pair(xv[u].z, xv[u].w, v.z, v.w);
+        xf[sl * 32 + L] = v;
+      }
+    }
   }
   __syncthreads();
 

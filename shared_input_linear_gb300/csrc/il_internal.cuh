@@ -192,7 +192,7 @@ struct Launch {
   cudaLaunchAttribute attr[3];
   int nattr = 0;
   std::shared_ptr<unsigned char> store;
-  void* args[16];
+  void* args[20];
   int nargs = 0;
 
   // Copies the arguments (each of the kernel's parameter type) into 64-byte
@@ -200,7 +200,7 @@ struct Launch {
   template <class... A>
   bool set_args(const A&... a) {
     constexpr size_t n = sizeof...(A);
-    static_assert(n >= 1 && n <= 16, "1 to 16 kernel arguments");
+    static_assert(n >= 1 && n <= 20, "1 to 20 kernel arguments");
     const size_t sizes[n] = {sizeof(A)...};
     const size_t aligns[n] = {alignof(A)...};
     const void* srcs[n] = {static_cast<const void*>(&a)...};

@@ -4,10 +4,13 @@
 // result is the first maximum.
 //
 //   1. cl = centroids . x               decode kernel (a one-job batch, t = 1)
-//   2. sel = top-k of cl                 topk_kernel: one CTA, bitonic sort of
-//                                        rank keys in shared memory
-//   3. score[i*per + j] =                cluster_score_kernel: one warp per
-//        embed[ordering[sel[i]*per+j]].x gathered row, bf16 x fp32 in fp32
+//   2. sel = top-k of cl                 k <= 32: inside the scoring kernel, every
+//                                        CTA for itself (select_score_kernel);
+//                                        larger k: topk_kernel, one CTA, radix
+//                                        select of rank keys in shared memory
+//   3. score[i*per + j] =                one warp per gathered row, bf16 x fp32
+//        embed[ordering[sel[i]*per+j]].x in fp32 (cluster_score_kernel after
+//                                        topk_kernel)
 //   4. first maximum                     same kernel: 64-bit keys, atomicMax per
 //                                        CTA, the last CTA to finish writes the token
 //
@@ -29,6 +32,8 @@ constexpr int kTopkThreads = 512;
 constexpr int kSelectMax = 4096;  // larger k sorts every key instead of selecting
 constexpr int kScoreThreads = 256;
 constexpr int kRowVecs = 16;  // rows up to 32 * 16 * 8 = 4096 wide are loaded in one go
+constexpr int kFusedK = 32;   // k up to this: selection inside the scoring kernel
+constexpr int kFusedThreads = 512;
 
 // fp32 -> u32 whose unsigned order is the float order (-inf lowest of the numbers).
 __device__ __forceinline__ uint32_t orderable(float v) {
@@ -157,24 +162,28 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   grid_dep_launch();
 }
 
-// Warp per gathered row; x staged once per CTA.  Each CTA folds its best key into
-// *best_key; the last CTA to finish turns it into the token and resets the state.
-__global__ void __launch_bounds__(kScoreThreads) cluster_score_kernel(
-    const float* __restrict__ x, int h, const uint16_t* __restrict__ embed, int64_t row_pitch,
-    const uint32_t* __restrict__ ordering, int64_t vocab, const uint32_t* __restrict__ sel, int k, int per,
-    float* __restrict__ scores_out, unsigned long long* best_key, unsigned* done, uint32_t* __restrict__ token_out,
-    float* __restrict__ score_out, unsigned* status) {
-  extern __shared__ float4 xs4[];
-  __shared__ unsigned long long warp_best[kScoreThreads / 32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  grid_dep_wait();  // sel comes from the previous kernel
+// x [h] -> shared memory as fp32 (h is a multiple of 8: bf16 weights are
+// uploaded only so, and h is their row length).
+__device__ __forceinline__ void stage_x(const float* __restrict__ x, int h, float4* xs4) {
   const float4* x4 = reinterpret_cast<const float4*>(x);
   for (int i = threadIdx.x; i < h / 4; i += blockDim.x) xs4[i] = x4[i];
-  __syncthreads();
+}
 
+// The exact logits of the k selected clusters' tokens, a warp per gathered row
+// (xs4: x staged in shared memory), and the first maximum.  Each CTA folds its
+// best key into *best_key; the last CTA to finish turns it into the token and
+// resets the state.  sel may be global or shared memory.
+template <int NW>
+__device__ __forceinline__ void score_rows(const float4* xs4, int h, const uint16_t* __restrict__ embed,
+                                           int64_t row_pitch, const uint32_t* __restrict__ ordering, int64_t vocab,
+                                           const uint32_t* sel, int k, int per, float* __restrict__ scores_out,
+                                           unsigned long long* best_key, unsigned* done,
+                                           uint32_t* __restrict__ token_out, float* __restrict__ score_out,
+                                           unsigned* status, unsigned long long* warp_best) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rows = k * per;
   unsigned long long best = 0ull;
-  for (int row = blockIdx.x * (kScoreThreads / 32) + warp; row < rows; row += gridDim.x * (kScoreThreads / 32)) {
+  for (int row = blockIdx.x * NW + warp; row < rows; row += gridDim.x * NW) {
     const int i = row / per, j = row - (row / per) * per;
     const uint32_t tok = ordering[(int64_t)sel[i] * per + j];
     const bool valid = (int64_t)tok < vocab;
@@ -223,7 +232,7 @@ __global__ void __launch_bounds__(kScoreThreads) cluster_score_kernel(
   __syncthreads();
   if (threadIdx.x == 0) {
     unsigned long long b = 0ull;
-    for (int w = 0; w < kScoreThreads / 32; ++w) b = warp_best[w] > b ? warp_best[w] : b;
+    for (int w = 0; w < NW; ++w) b = warp_best[w] > b ? warp_best[w] : b;
     if (b != 0ull) atomicMax(best_key, b);
     __threadfence();
     const unsigned prev = atomicAdd(done, 1u);
@@ -244,7 +253,154 @@ __global__ void __launch_bounds__(kScoreThreads) cluster_score_kernel(
       *done = 0u;
     }
   }
+}
+
+// Scoring after topk_kernel (k > kFusedK): x staged once per CTA.
+__global__ void __launch_bounds__(kScoreThreads) cluster_score_kernel(
+    const float* __restrict__ x, int h, const uint16_t* __restrict__ embed, int64_t row_pitch,
+    const uint32_t* __restrict__ ordering, int64_t vocab, const uint32_t* __restrict__ sel, int k, int per,
+    float* __restrict__ scores_out, unsigned long long* best_key, unsigned* done, uint32_t* __restrict__ token_out,
+    float* __restrict__ score_out, unsigned* status) {
+  extern __shared__ float4 xs4[];
+  __shared__ unsigned long long warp_best[kScoreThreads / 32];
+  grid_dep_wait();  // sel comes from the previous kernel
+  stage_x(x, h, xs4);
+  __syncthreads();
+  score_rows<kScoreThreads / 32>(xs4, h, embed, row_pitch, ordering, vocab, sel, k, per, scores_out, best_key, done,
+                                 token_out, score_out, status, warp_best);
   grid_dep_launch();
+}
+
+// ---- selection of at most 32 centroids inside the scoring kernel
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+  return a > b ? a : b;
+}
+__device__ __forceinline__ unsigned long long umin64(unsigned long long a, unsigned long long b) {
+  return a < b ? a : b;
+}
+
+// One key per lane, sorted descending over the lanes (lane 0 the largest): a
+// bitonic network whose blocks alternate direction until the last pass.
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long key, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, stride);
+      const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+      key = keep_max ? umax64(key, o) : umin64(key, o);
+    }
+  return key;
+}
+
+// A bitonic sequence over the lanes, sorted descending.
+__device__ __forceinline__ unsigned long long warp_merge_desc(unsigned long long key, int lane) {
+#pragma unroll
+  for (int stride = 16; stride > 0; stride >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, stride);
+    key = (lane & stride) == 0 ? umax64(key, o) : umin64(key, o);
+  }
+  return key;
+}
+
+// The 32 largest of two descending lists a and b (one key per lane): the lane-wise
+// maximum of a and reversed b is bitonic and holds them.
+__device__ __forceinline__ unsigned long long warp_top_of_two(unsigned long long a, unsigned long long b, int lane) {
+  return warp_merge_desc(umax64(a, __shfl_sync(0xffffffffu, b, 31 - lane)), lane);
+}
+
+// k <= kFusedK: every CTA selects the top k centroids itself (16 KB of logits from
+// L2) and scores its share of their rows -- one launch instead of two.
+//
+// Selection, exact for any input: (1) each lane's largest key over its share of
+// the n keys; each warp's two largest lane maxima; T = the least of those 32
+// values.  They come from 32 distinct lanes, each holding a key >= T, so at least
+// 32 keys are >= T and the top 32 are among them.  (2) Keys >= T are gathered in
+// shared memory, (3) sorted 32 at a time with a warp bitonic network into a
+// running top 32 per warp, (4) the warps' lists are merged pairwise.
+__global__ void __launch_bounds__(kFusedThreads, 1) select_score_kernel(
+    const float* __restrict__ x, int h, const float* __restrict__ cl, int n, const uint16_t* __restrict__ embed,
+    int64_t row_pitch, const uint32_t* __restrict__ ordering, int64_t vocab, uint32_t* __restrict__ sel_out, int k,
+    int per, float* __restrict__ scores_out, unsigned long long* best_key, unsigned* done,
+    uint32_t* __restrict__ token_out, float* __restrict__ score_out, unsigned* status) {
+  constexpr int NW = kFusedThreads / 32;
+  extern __shared__ float4 xs4[];  // x [h] | candidates [n]
+  __shared__ unsigned long long lists[NW][32];
+  __shared__ unsigned long long pair_min[NW];
+  __shared__ unsigned long long warp_best[NW];
+  __shared__ uint32_t sel[kFusedK];
+  __shared__ unsigned n_cand;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(xs4 + h / 4);
+
+  // x is this call's input, written before the previous kernel of the call began
+  stage_x(x, h, xs4);
+  if (threadIdx.x == 0) n_cand = 0u;
+  grid_dep_wait();  // cl comes from the previous kernel
+
+  // (1) threshold
+  unsigned long long lmax = 0ull;
+  for (int i = threadIdx.x; i < n; i += kFusedThreads) lmax = umax64(lmax, rank_key(__ldcg(cl + i), (uint32_t)i));
+  unsigned long long m1 = lmax, m2 = 0ull;  // the warp's two largest lane maxima
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long b1 = __shfl_xor_sync(0xffffffffu, m1, o), b2 = __shfl_xor_sync(0xffffffffu, m2, o);
+    m2 = umax64(umin64(m1, b1), umax64(m2, b2));
+    m1 = umax64(m1, b1);
+  }
+  if (lane == 0) pair_min[warp] = m2;
+  __syncthreads();
+  unsigned long long thr = pair_min[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) thr = umin64(thr, pair_min[w]);
+  // (2) gather the keys >= T (the logits are re-read from L2)
+  for (int base = 0; base < n; base += kFusedThreads) {
+    const int i = base + (int)threadIdx.x;
+    const unsigned long long key = i < n ? rank_key(__ldcg(cl + i), (uint32_t)i) : 0ull;
+    const bool take = i < n && key >= thr;
+    const unsigned ballot = __ballot_sync(0xffffffffu, take);
+    unsigned at = 0u;
+    if (lane == 0 && ballot != 0u) at = atomicAdd(&n_cand, (unsigned)__popc(ballot));
+    at = __shfl_sync(0xffffffffu, at, 0);
+    if (take) cand[at + __popc(ballot & ((1u << lane) - 1u))] = key;
+  }
+  __syncthreads();
+  // (3) running top 32 per warp over chunks of 32 candidates
+  const int nc = (int)n_cand;
+  const int chunks = (nc + 31) / 32;
+  const int nl = chunks < NW ? chunks : NW;  // lists that hold candidates
+  if (warp < nl) {
+    unsigned long long top = 0ull;
+    for (int c = warp; c < chunks; c += NW) {
+      const int e = c * 32 + lane;
+      const unsigned long long s = warp_sort_desc(e < nc ? cand[e] : 0ull, lane);
+      top = c == warp ? s : warp_top_of_two(top, s, lane);
+    }
+    lists[warp][lane] = top;
+  }
+  __syncthreads();
+  // (4) pairwise merge of the lists: list w takes list w + s
+  int span = 1;
+  while (span < nl) span <<= 1;
+  for (int s = span >> 1; s >= 1; s >>= 1) {
+    if (warp < s && warp + s < nl) {
+      const unsigned long long m = warp_top_of_two(lists[warp][lane], lists[warp + s][lane], lane);
+      __syncwarp();
+      lists[warp][lane] = m;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x < k) {
+    const uint32_t c = ~(uint32_t)lists[0][threadIdx.x];
+    sel[threadIdx.x] = c;
+    if (blockIdx.x == 0 && sel_out != nullptr) sel_out[threadIdx.x] = c;
+  }
+  __syncthreads();
+  // the next kernel may start; it waits for this one before reading its results
+  grid_dep_launch();
+  score_rows<NW>(xs4, h, embed, row_pitch, ordering, vocab, sel, k, per, scores_out, best_key, done, token_out,
+                 score_out, status, warp_best);
 }
 
 }  // namespace
@@ -259,6 +415,13 @@ size_t topk_smem(int n_cent, int k) {
   return k > kSelectMax ? (size_t)p * sizeof(unsigned long long)
                         : ((size_t)n_cent + (size_t)pk) * sizeof(unsigned long long);
 }
+
+// Dynamic shared memory of select_score_kernel: x, then the candidate keys (at
+// most every centroid).
+size_t fused_smem(int h, int n_cent) {
+  return (size_t)h * sizeof(float) + (size_t)n_cent * sizeof(unsigned long long);
+}
+constexpr size_t kFusedSmemMax = 200 * 1024;
 
 cudaError_t prepare_lmhead(const float* x, int h, const float* cl, int n_cent, int k, const PackedWeight& embed,
                            const uint32_t* ordering, int per, uint32_t* sel, float* scores_out,
@@ -276,8 +439,29 @@ cudaError_t prepare_lmhead(const float* x, int h, const float* cl, int n_cent, i
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(cluster_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)(kMaxHeadWidth * sizeof(float)));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(select_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kFusedSmemMax);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set.fetch_or(1ull << dev);
+  }
+  const int rows = k * per;
+  if (k <= kFusedK && fused_smem(h, n_cent) <= kFusedSmemMax) {
+    // one launch: every CTA selects, then scores its share of the rows
+    int grid = (rows + kFusedThreads / 32 - 1) / (kFusedThreads / 32);
+    if (grid > num_sms) grid = num_sms;
+    Launch f;
+    f.fn = reinterpret_cast<const void*>(select_score_kernel);
+    f.grid = dim3(grid);
+    f.block = dim3(kFusedThreads);
+    f.smem = fused_smem(h, n_cent);
+    if (kUsePdl) f.allow_early_start();
+    if (!f.set_args(x, h, cl, n_cent, reinterpret_cast<const uint16_t*>(embed.quants), (int64_t)embed.n_in_pad,
+                    ordering, (int64_t)embed.n_out, sel, k, per, scores_out, best_key, done, token_out, score_out,
+                    status))
+      return cudaErrorMemoryAllocation;
+    out->push_back(f);
+    return cudaSuccess;
   }
   Launch a;
   a.fn = reinterpret_cast<const void*>(topk_kernel);
@@ -287,7 +471,6 @@ cudaError_t prepare_lmhead(const float* x, int h, const float* cl, int n_cent, i
   if (kUsePdl) a.allow_early_start();
   if (!a.set_args(cl, n_cent, p, k, sel)) return cudaErrorMemoryAllocation;
 
-  const int rows = k * per;
   const int warps_per_cta = kScoreThreads / 32;
   int grid = (rows + warps_per_cta - 1) / warps_per_cta;
   if (grid > 4 * num_sms) grid = 4 * num_sms;

@@ -113,6 +113,44 @@ def test_integer_exact_ties(sil, seed, top_k):
     assert got["token"] == ref["token"] and got["score"] == ref["score"]
 
 
+@pytest.mark.parametrize("n_cent,top_k", [(4096, 32), (16384, 32), (700, 31), (33, 32), (4096, 33)])
+def test_equal_logits_take_the_lowest_indices(sil, n_cent, top_k):
+    # every centroid logit equal: the k lowest indices win, in order.  For k <= 32 this is
+    # the in-kernel selection's worst case (hundreds of keys pass its first threshold);
+    # k = 33 takes the separate selection kernel
+    rng = np.random.default_rng(n_cent + top_k)
+    h, per = 16, 2
+    vocab = n_cent * per
+    x = rng.integers(-1, 3, size=h)
+    cw = np.ones((n_cent, h))
+    ew = rng.integers(-2, 3, size=(vocab, h))
+    inp = _inputs(h, vocab, n_cent, x, cw, ew, rng.permutation(vocab))
+    ref = oracle.centroid_head(inp.centroids, n_cent, inp.embed, vocab, h, inp.ordering, inp.x, top_k)
+    got = _run(sil, inp, top_k)
+    assert list(got["sel"]) == list(range(min(top_k, n_cent))) == list(ref["sel"])
+    assert np.array_equal(got["scores"].astype(np.float64), ref["scores"])
+    assert got["token"] == ref["token"] and got["score"] == ref["score"]
+
+
+@pytest.mark.parametrize("h,top_k", [(104, 8), (40, 40), (8, 3), (2568, 32), (4104, 5)])
+def test_ragged_head_widths(sil, h, top_k):
+    # widths that are a multiple of 8 (bf16 weights need it) but of no larger power of
+    # two: a row ends mid-way through a lane's 16-byte vectors; integer data keeps every
+    # decision exact (4104 > 4096 takes the row loop that does not hold a row in registers)
+    rng = np.random.default_rng(h)
+    n_cent, per = 48, 4
+    vocab = n_cent * per
+    x = rng.integers(-1, 3, size=h)
+    cw = rng.integers(-1, 2, size=(n_cent, h))
+    ew = rng.integers(-1, 2, size=(vocab, h))
+    inp = _inputs(h, vocab, n_cent, x, cw, ew, rng.permutation(vocab))
+    ref = oracle.centroid_head(inp.centroids, n_cent, inp.embed, vocab, h, inp.ordering, inp.x, top_k)
+    got = _run(sil, inp, top_k)
+    assert list(got["sel"]) == list(ref["sel"])
+    assert np.array_equal(got["scores"].astype(np.float64), ref["scores"])
+    assert got["token"] == ref["token"] and got["score"] == ref["score"]
+
+
 def test_nan_centroid_and_no_winner(sil):
     # a NaN centroid logit ranks last; when every logit is NaN the token is 0 and the score -inf
     h, n_cent, per = 16, 4, 2
