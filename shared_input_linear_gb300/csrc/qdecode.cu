@@ -55,6 +55,7 @@ constexpr int kMaxStageRecords = 4;
 // cross-CTA sum through the workspace ends every split tile).
 constexpr double kSplitPenalty = 0.03;
 constexpr int kSlotRounds = 2;          // partial-sum slots per warp row: rounds a warp may run ahead
+constexpr int kXRegUnits = 6;          // x units per thread staged in one pass from registers
 constexpr unsigned kStQDecode = 0x10;   // a wait for a record gave up
 constexpr unsigned kStQSlot = 0x20;     // a wait for a free partial-sum slot gave up
 
@@ -303,80 +304,90 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
   // unit of 512 bytes per pair of slots, lane L's 16 bytes at 16 L holding its B
   // fragment of both slots: TT = 8, the fp16 of token L/4; TT = 4, the fp16 high
   // part (L/4 < 4) or the fp16 rounding of the remainder (L/4 >= 4) of token
-  // (L/4) % 4.  Lanes of tokens >= t hold zeros.
-  // (loads are issued 8 at a time before they are used: x comes from L2, and a
-  // chain of dependent loads would hold every warp up before the first record)
-  const int c4n = ns * F::CK / 4;
-  {
-    const int c4max = min(c4n, (p.n_in - cb * F::CK) / 4);  // float4s inside n_in
-    const float4* xr4 = reinterpret_cast<const float4*>(p.x + (size_t)cb * F::CK);
-    float mx[TT];
-#pragma unroll
-    for (int tk = 0; tk < TT; ++tk) mx[tk] = 0.f;
-    // every token's float4 of a column block in flight at once
-#pragma unroll 2
-    for (int c4 = threadIdx.x; c4 < c4max; c4 += kQThreads) {
-      float4 v[TT];
-#pragma unroll
-      for (int tk = 0; tk < TT; ++tk)
-        v[tk] = tk < p.t ? __ldg(xr4 + (size_t)tk * (p.x_row_stride / 4) + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int tk = 0; tk < TT; ++tk)
-        mx[tk] = fmaxf(mx[tk], fmaxf(fmaxf(fabsf(v[tk].x), fabsf(v[tk].y)), fmaxf(fabsf(v[tk].z), fabsf(v[tk].w))));
-    }
-#pragma unroll
-    for (int tk = 0; tk < TT; ++tk) {
-      float m = mx[tk];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0 && m > 0.f) atomicMax(&tok_max[tk], __float_as_uint(m));  // non-negative: bits order as values
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x < 8) tok_scale[threadIdx.x] = ldexpf(1.0f, -x_exponent(tok_max[threadIdx.x]));
-  __syncthreads();
+  // (L/4) % 4.  Lanes of tokens >= t hold zeros.  Thread i always serves lane
+  // i % 32 of its units, so it sees a single token.
   constexpr int kSlotsPerUnit = 2;
-  constexpr int kUnroll = 4;
   const int n_el = ns * (F::SLOTS / kSlotsPerUnit) * 32;
-  for (int e0 = threadIdx.x; e0 < n_el; e0 += kUnroll * kQThreads) {
-    float4 v[kUnroll][kSlotsPerUnit];
+  const int my_tk = TT == 8 ? (lane >> 2) : ((lane >> 2) & 3);
+  const bool my_low = TT == 4 && (lane >> 2) >= 4;
+  auto load_unit = [&](int e, float4 (&v)[kSlotsPerUnit]) {
+    const int unit = e >> 5;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int e = e0 + u * kQThreads;
-      const int L = e & 31, unit = e >> 5;
-      const int tk = TT == 8 ? (L >> 2) : ((L >> 2) & 3);
+    for (int h = 0; h < kSlotsPerUnit; ++h) {
+      const int col = cb * F::CK + 16 * (unit * kSlotsPerUnit + h) + 4 * (lane & 3);
+      v[h] = (e < n_el && my_tk < p.t && col < p.n_in)
+                 ? __ldg(reinterpret_cast<const float4*>(p.x + (size_t)my_tk * p.x_row_stride + col))
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  auto store_unit = [&](int e, const float4 (&v)[kSlotsPerUnit], float xsc) {
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (my_tk < p.t) {
 #pragma unroll
       for (int h = 0; h < kSlotsPerUnit; ++h) {
-        const int col = cb * F::CK + 16 * (unit * kSlotsPerUnit + h) + 4 * (L & 3);
-        v[u][h] = (e < n_el && tk < p.t && col < p.n_in)
-                      ? __ldg(reinterpret_cast<const float4*>(p.x + (size_t)tk * p.x_row_stride + col))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 x4 = v[h];
+        const __half2 h01 = __floats2half2_rn(x4.x * xsc, x4.y * xsc);
+        const __half2 h23 = __floats2half2_rn(x4.z * xsc, x4.w * xsc);
+        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        const __half2 l01 = __floats2half2_rn(x4.x * xsc - f01.x, x4.y * xsc - f01.y);
+        const __half2 l23 = __floats2half2_rn(x4.z * xsc - f23.x, x4.w * xsc - f23.y);
+        w[2 * h] = my_low ? h2_bits(l01) : h2_bits(h01);
+        w[2 * h + 1] = my_low ? h2_bits(l23) : h2_bits(h23);
       }
     }
+    *reinterpret_cast<uint4*>(xs + (size_t)(e >> 5) * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  };
+  // the token's largest |x| over this warp's lanes of that token -> tok_max
+  auto fold_max = [&](float m) {
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int e = e0 + u * kQThreads;
-      if (e >= n_el) break;
-      const int L = e & 31, unit = e >> 5;
-      const int gg = L >> 2;
-      const int tk = TT == 8 ? gg : (gg & 3);
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
-      if (tk < p.t) {
-        const float xsc = tok_scale[tk];
+    for (int o = 1; o < 4; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (TT == 4) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+    if ((lane & 3) == 0 && (TT == 8 || lane < 16) && m > 0.f)
+      atomicMax(&tok_max[my_tk], __float_as_uint(m));  // non-negative: bits order as values
+  };
+  auto amax4 = [](const float4& a) { return fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))); };
+  if (n_el <= kXRegUnits * kQThreads) {
+    // one pass over global memory: every unit of this thread in registers (all
+    // loads in flight at once: x comes from L2 behind the weight stream), the
+    // token maxima, then the conversion from registers
+    float4 v[kXRegUnits][kSlotsPerUnit];
+    float m = 0.f;
 #pragma unroll
-        for (int h = 0; h < kSlotsPerUnit; ++h) {
-          const float4 x4 = v[u][h];
-          const __half2 h01 = __floats2half2_rn(x4.x * xsc, x4.y * xsc);
-          const __half2 h23 = __floats2half2_rn(x4.z * xsc, x4.w * xsc);
-          const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-          const __half2 l01 = __floats2half2_rn(x4.x * xsc - f01.x, x4.y * xsc - f01.y);
-          const __half2 l23 = __floats2half2_rn(x4.z * xsc - f23.x, x4.w * xsc - f23.y);
-          const bool low = TT == 4 && gg >= 4;
-          w[2 * h] = low ? h2_bits(l01) : h2_bits(h01);
-          w[2 * h + 1] = low ? h2_bits(l23) : h2_bits(h23);
-        }
-      }
-      *reinterpret_cast<uint4*>(xs + (size_t)unit * 512 + L * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int u = 0; u < kXRegUnits; ++u) load_unit(threadIdx.x + u * kQThreads, v[u]);
+#pragma unroll
+    for (int u = 0; u < kXRegUnits; ++u) m = fmaxf(m, fmaxf(amax4(v[u][0]), amax4(v[u][1])));
+    fold_max(m);
+    __syncthreads();
+    if (threadIdx.x < 8) tok_scale[threadIdx.x] = ldexpf(1.0f, -x_exponent(tok_max[threadIdx.x]));
+    __syncthreads();
+    const float xsc = tok_scale[my_tk];
+#pragma unroll
+    for (int u = 0; u < kXRegUnits; ++u)
+      if (threadIdx.x + u * kQThreads < n_el) store_unit(threadIdx.x + u * kQThreads, v[u], xsc);
+  } else {
+    // larger slices: the maxima in a first pass, the conversion in a second
+    // (loads issued kUnroll units at a time)
+    constexpr int kUnroll = 4;
+    float m = 0.f;
+    for (int e0 = threadIdx.x; e0 < n_el; e0 += kUnroll * kQThreads) {
+      float4 v[kUnroll][kSlotsPerUnit];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) load_unit(e0 + u * kQThreads, v[u]);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) m = fmaxf(m, fmaxf(amax4(v[u][0]), amax4(v[u][1])));
+    }
+    fold_max(m);
+    __syncthreads();
+    if (threadIdx.x < 8) tok_scale[threadIdx.x] = ldexpf(1.0f, -x_exponent(tok_max[threadIdx.x]));
+    __syncthreads();
+    const float xsc = tok_scale[my_tk];
+    for (int e0 = threadIdx.x; e0 < n_el; e0 += kUnroll * kQThreads) {
+      float4 v[kUnroll][kSlotsPerUnit];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) load_unit(e0 + u * kQThreads, v[u]);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (e0 + u * kQThreads < n_el) store_unit(e0 + u * kQThreads, v[u], xsc);
     }
   }
   __syncthreads();
