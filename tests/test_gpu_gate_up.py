@@ -74,6 +74,19 @@ def test_gate_up_parity(sil, fmt, t, n_in, n_out):
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+def test_gate_up_tensor_core_long_k(sil, fmt):
+    # a fused job with long K over 22 row tiles of interleaved gate/up rows on the
+    # tensor-core kernel, element-wise
+    n_in, n_out, t = 8192, 1400, 17
+    x, gate, up = _draw(fmt, n_in, n_out, t, seed=29)
+    w = sil.upload_gate_up(fmt, gate, up, n_out, n_in)
+    (h,), guards = _run(sil, [w], x, t, [n_out])
+    w.free()
+    assert guards, "a kernel wrote outside h"
+    _assert_gate_up(fmt, gate, up, n_out, n_in, x, h, "gate_up long K")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
 def test_gate_up_dequant_interleaves_rows(sil, fmt):
     import torch
     n_in, n_out = 256, 40

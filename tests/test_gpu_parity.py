@@ -99,6 +99,17 @@ def test_tensor_core_shapes(sil, fmt, t, n_in, n_outs):
     assert_parity(b, ys, "tensor-core shapes")
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "q8", "q4"])
+@pytest.mark.parametrize("t,n_in,n_outs", [(17, 8192, (1500, 1100)), (260, 4096, (2600,))])
+def test_tensor_core_long_k(sil, fmt, t, n_in, n_outs):
+    # long K over many row tiles, element-wise: t = 17 on 128-token tiles (t fits
+    # one), t = 260 on two or three token tiles with a ragged last one
+    b = wl.make_batch(n_in, n_outs, t, fmt, seed=t + len(n_outs))
+    ys, guards = run(sil, b)
+    assert guards
+    assert_parity(b, ys, "long K")
+
+
 def test_stream_k_growing_tile_counts(sil):
     # consecutive tensor-core batches on one stream whose tile counts grow: the
     # per-tile arrival counters of the split tiles must start at zero every time
