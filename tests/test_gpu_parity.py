@@ -124,6 +124,35 @@ def test_stream_k_growing_tile_counts(sil):
         assert_parity_sampled(b, ys, n_samples=128, what=f"{fmt} t={t} n_out={n_out}")
 
 
+def test_decode_back_to_back_launches(sil):
+    # Q8/Q4 decode launches of varied size and K split queued on one stream without a
+    # sync in between (each may start behind the previous one): the per-tile counters
+    # of split tiles are back at zero for every launch, and every output is written
+    import torch
+    s = torch.cuda.Stream()
+    cases = []
+    for fmt, t, n_in, n_out in (("q8", 1, 4096, 24576), ("q4", 3, 4096, 24576), ("q8", 8, 2560, 40000),
+                                ("q4", 1, 2560, 65536), ("q8", 5, 4096, 24576), ("q4", 8, 12288, 8192)):
+        b = wl.make_batch(n_in, (n_out,), t, fmt, seed=t + n_out)
+        w = upload(sil, b)
+        x = torch.from_numpy(b.x).cuda()
+        ys = [torch.full((t, n_out), float("nan"), device="cuda") for _ in range(2)]
+        cases.append((b, w, x, ys))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for rep in range(2):
+            for b, w, x, ys in cases:
+                sil.matmul_batch(x, [(w[0], ys[rep])], stream=s)
+    torch.cuda.synchronize()
+    for b, w, x, ys in cases:
+        for y in ys:
+            # every output written (a tile no warp took would keep its NaNs), then sampled parity
+            assert not bool(torch.isnan(y).any()), f"{b.fmt} t={b.t}: outputs left unwritten"
+            assert_parity_sampled(b, [y.cpu().numpy()], n_samples=256, what=f"{b.fmt} t={b.t}")
+        for wi in w:
+            wi.free()
+
+
 def test_bf16_odd_k(sil):
     # bf16 allows any n_in that is a multiple of 8
     for n_in in (8, 40, 264):
