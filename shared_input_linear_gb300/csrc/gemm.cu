@@ -560,27 +560,45 @@ __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid
 }
 
 // x fp32 [t][n_in] -> bf16 [t][n_in_pad] (round to nearest even), 0 in the padding.
-__global__ void cast_bf16_kernel(const float* __restrict__ x, int64_t t, int64_t n_in, int64_t n_in_pad,
-                                 __nv_bfloat16* __restrict__ out) {
+// One resident wave of CTAs; each thread keeps kCastUnroll vectors of 8 columns in
+// flight (all loads issued before the first store).
+constexpr int kCastUnroll = 4;
+__global__ void __launch_bounds__(256) cast_bf16_kernel(const float* __restrict__ x, int64_t t, int64_t n_in,
+                                                        int64_t n_in_pad, __nv_bfloat16* __restrict__ out) {
   const int64_t per_row = n_in_pad / 8;
   const int64_t total = t * per_row;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   grid_dep_wait();
-  for (int64_t v = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v < total;
-       v += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = v / per_row;
-    const int64_t k = (v - r * per_row) * 8;
-    uint4 o = make_uint4(0, 0, 0, 0);
-    if (k < n_in) {  // n_in is a multiple of 8: the 8 columns are all inside or all outside
-      const float4 a = *reinterpret_cast<const float4*>(x + r * n_in + k);
-      const float4 b = *reinterpret_cast<const float4*>(x + r * n_in + k + 4);
-      __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y), h1 = __floats2bfloat162_rn(a.z, a.w);
-      __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y), h3 = __floats2bfloat162_rn(b.z, b.w);
+  for (int64_t v0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; v0 < total; v0 += kCastUnroll * stride) {
+    float4 a[kCastUnroll], b[kCastUnroll];
+#pragma unroll
+    for (int u = 0; u < kCastUnroll; ++u) {
+      const int64_t v = v0 + u * stride;
+      a[u] = b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (v < total) {
+        const int64_t r = v / per_row;
+        const int64_t k = (v - r * per_row) * 8;
+        if (k < n_in) {  // n_in is a multiple of 8: the 8 columns are all inside or all outside
+          a[u] = __ldcs(reinterpret_cast<const float4*>(x + r * n_in + k));
+          b[u] = __ldcs(reinterpret_cast<const float4*>(x + r * n_in + k + 4));
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCastUnroll; ++u) {
+      const int64_t v = v0 + u * stride;
+      if (v >= total) break;
+      const int64_t r = v / per_row;
+      const int64_t k = (v - r * per_row) * 8;
+      __nv_bfloat162 h0 = __floats2bfloat162_rn(a[u].x, a[u].y), h1 = __floats2bfloat162_rn(a[u].z, a[u].w);
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(b[u].x, b[u].y), h3 = __floats2bfloat162_rn(b[u].z, b[u].w);
+      uint4 o;
       o.x = *reinterpret_cast<uint32_t*>(&h0);
       o.y = *reinterpret_cast<uint32_t*>(&h1);
       o.z = *reinterpret_cast<uint32_t*>(&h2);
       o.w = *reinterpret_cast<uint32_t*>(&h3);
+      *reinterpret_cast<uint4*>(out + r * n_in_pad + k) = o;
     }
-    *reinterpret_cast<uint4*>(out + r * n_in_pad + k) = o;
   }
   grid_dep_launch();
 }
@@ -628,19 +646,21 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int grid_cast(int64_t work) {
+int grid_cast(int64_t work, int num_sms) {
+  // 8 CTAs of 256 threads fill an SM; more than one wave only adds scheduling
   int64_t g = (work + 255) / 256;
-  if (g > 4096) g = 4096;
+  const int64_t wave = 8LL * (num_sms > 0 ? num_sms : 1);
+  if (g > wave) g = wave;
   return (int)(g < 1 ? 1 : g);
 }
 
 }  // namespace
 
 cudaError_t prepare_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_in_pad, __nv_bfloat16* out,
-                              Launch* L) {
+                              int num_sms, Launch* L) {
   *L = Launch();
   L->fn = reinterpret_cast<const void*>(cast_bf16_kernel);
-  L->grid = dim3(grid_cast(t * (n_in_pad / 8)));
+  L->grid = dim3(grid_cast(t * (n_in_pad / 8), num_sms));
   L->block = dim3(256);
   if (kUsePdl) L->allow_early_start();
   if (!L->set_args(x, t, n_in, n_in_pad, out)) return cudaErrorMemoryAllocation;

@@ -742,7 +742,7 @@ cudaError_t prepare_batch(const BatchPlan& plan, const float* x, int64_t t, int6
   if (plan.xb_bytes > 0) {
     if (xb == nullptr) return cudaErrorInvalidValue;
     Launch cast;
-    cudaError_t e = prepare_cast_bf16(x, t, n_in, plan.n_in_pad, xb, &cast);
+    cudaError_t e = prepare_cast_bf16(x, t, n_in, plan.n_in_pad, xb, num_sms, &cast);
     if (e != cudaSuccess) return e;
     out->push_back(cast);
     for (int f = 0; f < 3; ++f)

@@ -256,7 +256,7 @@ cudaError_t prepare_qdecode(int fmt, const DecodeParams& p, int num_sms, unsigne
 // (0: none).
 size_t qdecode_workspace_bytes(int fmt, const DecodeParams& p, int num_sms);
 cudaError_t prepare_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n_in_pad, __nv_bfloat16* out,
-                              Launch* L);
+                              int num_sms, Launch* L);
 
 // Token counts from which a batch takes the tensor-core path instead of the
 // decode kernel (which streams the weights once per 8 tokens).
