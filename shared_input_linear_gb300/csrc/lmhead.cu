@@ -34,6 +34,7 @@ constexpr int kScoreThreads = 256;
 constexpr int kRowVecs = 16;  // rows up to 32 * 16 * 8 = 4096 wide are loaded in one go
 constexpr int kFusedK = 32;   // k up to this: selection inside the scoring kernel
 constexpr int kFusedThreads = 512;
+constexpr int kKeyRegs = 8;  // centroid keys per thread held in registers by the selection
 
 // fp32 -> u32 whose unsigned order is the float order (-inf lowest of the numbers).
 __device__ __forceinline__ uint32_t orderable(float v) {
@@ -339,9 +340,20 @@ __global__ void __launch_bounds__(kFusedThreads, 1) select_score_kernel(
   if (threadIdx.x == 0) n_cand = 0u;
   grid_dep_wait();  // cl comes from the previous kernel
 
-  // (1) threshold
+  // (1) threshold.  The first kKeyRegs * 512 keys stay in registers for the gather
+  // (all their loads in flight at once); keys past them are read again from L2.
+  unsigned long long kr[kKeyRegs];
+#pragma unroll
+  for (int u = 0; u < kKeyRegs; ++u) {
+    const int i = (int)threadIdx.x + u * kFusedThreads;
+    const float v = i < n ? __ldcg(cl + i) : 0.f;
+    kr[u] = i < n ? rank_key(v, (uint32_t)i) : 0ull;
+  }
   unsigned long long lmax = 0ull;
-  for (int i = threadIdx.x; i < n; i += kFusedThreads) lmax = umax64(lmax, rank_key(__ldcg(cl + i), (uint32_t)i));
+#pragma unroll
+  for (int u = 0; u < kKeyRegs; ++u) lmax = umax64(lmax, kr[u]);
+  for (int i = (int)threadIdx.x + kKeyRegs * kFusedThreads; i < n; i += kFusedThreads)
+    lmax = umax64(lmax, rank_key(__ldcg(cl + i), (uint32_t)i));
   unsigned long long m1 = lmax, m2 = 0ull;  // the warp's two largest lane maxima
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -354,16 +366,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1) select_score_kernel(
   unsigned long long thr = pair_min[0];
 #pragma unroll
   for (int w = 1; w < NW; ++w) thr = umin64(thr, pair_min[w]);
-  // (2) gather the keys >= T (the logits are re-read from L2)
-  for (int base = 0; base < n; base += kFusedThreads) {
-    const int i = base + (int)threadIdx.x;
-    const unsigned long long key = i < n ? rank_key(__ldcg(cl + i), (uint32_t)i) : 0ull;
-    const bool take = i < n && key >= thr;
+  // (2) gather the keys >= T (0 pads past n and is never >= T: T is a real key or 0,
+  // and real keys are not 0 -- see rank_key)
+  auto gather = [&](unsigned long long key, bool real) {
+    const bool take = real && key >= thr;
     const unsigned ballot = __ballot_sync(0xffffffffu, take);
     unsigned at = 0u;
     if (lane == 0 && ballot != 0u) at = atomicAdd(&n_cand, (unsigned)__popc(ballot));
     at = __shfl_sync(0xffffffffu, at, 0);
     if (take) cand[at + __popc(ballot & ((1u << lane) - 1u))] = key;
+  };
+#pragma unroll
+  for (int u = 0; u < kKeyRegs; ++u)
+    if (u * kFusedThreads < n) gather(kr[u], (int)threadIdx.x + u * kFusedThreads < n);
+  for (int base = kKeyRegs * kFusedThreads; base < n; base += kFusedThreads) {
+    const int i = base + (int)threadIdx.x;
+    gather(i < n ? rank_key(__ldcg(cl + i), (uint32_t)i) : 0ull, i < n);
   }
   __syncthreads();
   // (3) running top 32 per warp over chunks of 32 candidates
