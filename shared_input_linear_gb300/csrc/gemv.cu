@@ -24,6 +24,8 @@
 //    the resident clusters in whole rounds (a part-full last round idles SMs).
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include <mutex>
 #include <map>
 #include <tuple>
@@ -39,6 +41,8 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSliceK = 4096;  // columns of x staged per CTA (32 bytes each)
 constexpr int kStageUnroll = 4;   // x loads in flight per thread while staging
+constexpr size_t kTwoCtaSmem = 100 * 1024;  // dynamic shared memory that still fits two CTAs per SM
+constexpr int kMaxPrefetch = 3;   // weight batches per warp staged in shared memory before the wait
 
 // Not volatile: independent MMAs (different accumulators) may be interleaved by
 // the scheduler, which hides the tensor-pipe latency of each accumulate chain.
@@ -49,6 +53,15 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint4& a, uint32_t
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
+
+// 16-byte asynchronous copy global -> shared (L2 only), completed by cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // (hi pair, lo pair) of two fp32 values: hi = bf16_rn(v), lo = bf16_rn(v - hi).
 __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -93,6 +106,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
   const int slots = p.chunks_per_slice * kSlotsPerChunk;
   uint4* xf = reinterpret_cast<uint4*>(smem);
   float* red = reinterpret_cast<float*>(smem + (size_t)slots * 512);
+  // batches staged in shared memory ahead of the register pair: [warp][P][B][G][32 lanes]
+  uint4* pre = reinterpret_cast<uint4*>(smem + (size_t)slots * 512 + (CLUSTER ? 2 * GPB * 64 * sizeof(float) : 0)) +
+               (size_t)warp * p.prefetch * B * G * 32;
 
   // ---- load cursor: base pointers of this warp's G groups in the row block
   // being loaded.  A group past the last job (a partial row block) streams
@@ -115,22 +131,51 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
   // always in flight while the other is consumed.
   int l_rb = 0, l_b = 0;
   set_load_rb(0);
-  auto load_batch = [&](uint4 (&dq)[B][G]) {
-#pragma unroll
-    for (int i = 0; i < B; ++i)
-#pragma unroll
-      for (int g = 0; g < G; ++g) dq[i][g] = __ldg(reinterpret_cast<const uint4*>(lw[g] + (l_b * B + i) * kWStep));
+  auto advance = [&]() {
     if (++l_b == nb) {
       l_b = 0;
       set_load_rb(++l_rb);
     }
   };
+  auto load_batch = [&](uint4 (&dq)[B][G]) {
+#pragma unroll
+    for (int i = 0; i < B; ++i)
+#pragma unroll
+      for (int g = 0; g < G; ++g) dq[i][g] = __ldg(reinterpret_cast<const uint4*>(lw[g] + (l_b * B + i) * kWStep));
+    advance();
+  };
 
   uint4 qa[B][G], qb[B][G];
   // Start the weight stream before staging x so HBM is busy from the first cycle;
-  // the weights do not depend on the previous kernel, x may.
+  // the weights do not depend on the previous kernel, x may.  Two batches go to the
+  // registers, the next p.prefetch batches to shared memory by asynchronous copies
+  // (the launch waits ~2 us for the previous kernel to finish and flush).
   if (total > 0) load_batch(qa);
   if (total > 1) load_batch(qb);
+  const int n_pre = max(0, min(p.prefetch, total - 2));
+  for (int k = 0; k < n_pre; ++k) {
+#pragma unroll
+    for (int i = 0; i < B; ++i)
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        cp_async16(pre + ((k * B + i) * G + g) * 32 + lane, lw[g] + (l_b * B + i) * kWStep);
+    advance();
+  }
+  cp_async_commit();
+  int fetched = 2;  // batches handed to the register pair so far
+  auto next_batch = [&](uint4 (&dq)[B][G]) {
+    const int k = fetched - 2;
+    if (k < n_pre) {
+      if (k == 0) cp_async_wait_all();  // this lane's staged copies have landed
+#pragma unroll
+      for (int i = 0; i < B; ++i)
+#pragma unroll
+        for (int g = 0; g < G; ++g) dq[i][g] = pre[((k * B + i) * G + g) * 32 + lane];
+    } else {
+      load_batch(dq);
+    }
+    ++fetched;
+  };
   grid_dep_wait();
   // the next kernel may now be scheduled; it waits for this one before touching x or y
   grid_dep_launch();
@@ -266,10 +311,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const __grid_consta
 
   for (int bi = 0; bi < total; bi += 2) {
     consume(qa);
-    if (bi + 2 < total) load_batch(qa);
+    if (bi + 2 < total) next_batch(qa);
     if (bi + 1 < total) {
       consume(qb);
-      if (bi + 3 < total) load_batch(qb);
+      if (bi + 3 < total) next_batch(qb);
     }
   }
   if (CLUSTER) cg::this_cluster().sync();  // keep shared memory alive for remote readers
@@ -320,7 +365,7 @@ cudaError_t prepare_decode_bf16(const DecodeParams& pin, int num_sms, Launch* ou
       const int ce = (p.n_chunks + cp - 1) / cp;
       if (ce != c) continue;
       const size_t sm = (size_t)cp * spc * 512 + (c > 1 ? 2 * kWarps * g * 64 * sizeof(float) : 0);
-      const int slots = (sm <= 100 * 1024 ? 2 : 1) * num_sms;
+      const int slots = (sm <= kTwoCtaSmem ? 2 : 1) * num_sms;
       const int clusters = slots / c;
       if (clusters < 1) continue;
       const int rounds = (rowblocks + clusters - 1) / clusters;
@@ -341,7 +386,12 @@ cudaError_t prepare_decode_bf16(const DecodeParams& pin, int num_sms, Launch* ou
   p.slices = C;
   p.chunks_per_slice = cps;
   const bool cluster = C > 1;
-  const size_t smem = (size_t)cps * spc * 512 + (cluster ? 2 * gpb * 64 * sizeof(float) : 0);
+  const size_t smem_x = (size_t)cps * spc * 512 + (cluster ? 2 * gpb * 64 * sizeof(float) : 0);
+  // weight batches staged in shared memory before the wait, as many as keep two CTAs
+  // on an SM (the next launch's CTAs take the slots the previous launch frees)
+  const size_t per_batch = (size_t)kWarps * kBatchChunks * G * 512;
+  p.prefetch = smem_x <= kTwoCtaSmem ? (int)std::min<size_t>(kMaxPrefetch, (kTwoCtaSmem - smem_x) / per_batch) : 0;
+  const size_t smem = smem_x + (size_t)p.prefetch * per_batch;
 
   KernelFn fn = select(G, cluster);
   if (fn == nullptr) return cudaErrorInvalidValue;

@@ -99,6 +99,7 @@ struct DecodeParams {
   int total_groups;
   int n_rowblocks;
   int n_jobs;
+  int prefetch;          // bf16 decode: weight batches per warp staged in shared memory before the wait
   DecodeJob jobs[kMaxDecodeJobs];
 };
 
