@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define IL_VERSION 1
+#define IL_VERSION 2
 
 /* Storage format of a weight (oxinfer src/gpu.rs, enum WeightRef). */
 typedef enum { IL_BF16 = 0, IL_Q8 = 1, IL_Q4 = 2 } il_format;
@@ -77,6 +77,8 @@ typedef struct {
   uint64_t weight_bytes;      /* weight bytes those batches streamed      */
   uint64_t flops;             /* 2 * t * n_in * rows summed over jobs     */
   uint64_t errors;            /* calls that returned an error             */
+  uint64_t profiled_batches;  /* IL_PROFILE=1: calls whose device time is in device_ns */
+  uint64_t device_ns;         /* IL_PROFILE=1: their summed device time (ns)           */
 } il_stats;
 
 /*
@@ -267,8 +269,16 @@ const char* il_last_error(void);
  * il_upload_weight returned NULL.  Each entry point clears it on entry. */
 int il_last_status(void);
 
-/* Copies the cumulative counters into *out. */
+/* Copies the cumulative counters into *out (the page's `Backend::stats`, a
+ * cumulative timing summary when profiling).  With IL_PROFILE=1 in the
+ * environment, il_matmul_batch and il_centroid_head record a CUDA event before
+ * and after their launches on their stream (not while the stream is being
+ * captured, and not il_matmul_batch_noalloc); il_get_stats then waits for every
+ * recorded call to finish and adds its device time to device_ns.  Without
+ * IL_PROFILE nothing is recorded and nothing waits.  The entry points also mark
+ * their host work with NVTX ranges, which cost nothing unless a tool listens. */
 int il_get_stats(il_stats* out);
+/* Zeroes the counters (with IL_PROFILE=1, after waiting for the recorded calls). */
 void il_reset_stats(void);
 
 /* IL_VERSION of the loaded library. */

@@ -47,7 +47,7 @@ class _Job(ctypes.Structure):
 class _Stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in
                 ("uploads", "upload_bytes", "batches", "jobs", "launches", "weight_bytes",
-                 "flops", "errors")]
+                 "flops", "errors", "profiled_batches", "device_ns")]
 
 
 _lib = None

@@ -20,6 +20,8 @@
 #include <vector>
 #include <algorithm>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "il_internal.cuh"
 
 using namespace il;
@@ -41,8 +43,83 @@ void clear_error() {
 
 struct Stats {
   std::atomic<uint64_t> uploads{0}, upload_bytes{0}, batches{0}, jobs{0}, launches{0},
-      weight_bytes{0}, flops{0}, errors{0};
+      weight_bytes{0}, flops{0}, errors{0}, profiled_batches{0}, device_ns{0};
 } g_stats;
+
+// ---- optional timing (IL_PROFILE=1): CUDA events around each call's launches
+// on its stream; il_get_stats waits for the recorded calls and adds their device
+// time.  Calls on a stream that is being captured are not timed.
+bool profiling() {
+  static const bool on = [] {
+    const char* e = getenv("IL_PROFILE");
+    return e != nullptr && e[0] == '1';
+  }();
+  return on;
+}
+
+struct TimedCall {
+  cudaEvent_t begin, end;
+};
+std::mutex g_prof_mu;
+std::vector<TimedCall> g_prof;  // recorded, not yet added to the counters
+constexpr size_t kMaxPendingTimes = 4096;
+
+// Adds the device time of every recorded call (waits for each) and frees its events.
+void drain_times() {
+  std::vector<TimedCall> v;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    v.swap(g_prof);
+  }
+  for (const TimedCall& c : v) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(c.end) == cudaSuccess && cudaEventElapsedTime(&ms, c.begin, c.end) == cudaSuccess) {
+      g_stats.profiled_batches.fetch_add(1);
+      g_stats.device_ns.fetch_add((uint64_t)((double)ms * 1e6));
+    }
+    cudaEventDestroy(c.begin);
+    cudaEventDestroy(c.end);
+  }
+}
+
+// run_launches, timed when IL_PROFILE=1 (and the stream is not being captured).
+cudaError_t run_timed(const std::vector<Launch>& v, cudaStream_t stream, int* launches) {
+  TimedCall c{nullptr, nullptr};
+  bool timed = false;
+  if (profiling()) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone &&
+        cudaEventCreate(&c.begin) == cudaSuccess) {
+      if (cudaEventCreate(&c.end) == cudaSuccess) {
+        timed = cudaEventRecord(c.begin, stream) == cudaSuccess;
+      } else {
+        cudaEventDestroy(c.begin);
+      }
+    }
+  }
+  const cudaError_t e = run_launches(v, stream, launches);
+  if (timed) {
+    if (e == cudaSuccess && cudaEventRecord(c.end, stream) == cudaSuccess) {
+      size_t pending;
+      {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        g_prof.push_back(c);
+        pending = g_prof.size();
+      }
+      if (pending > kMaxPendingTimes) drain_times();
+    } else {
+      cudaEventDestroy(c.begin);
+      cudaEventDestroy(c.end);
+    }
+  }
+  return e;
+}
+
+// NVTX range over an entry point's host work (no-op unless a tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 std::mutex g_reg_mu;
 std::unordered_set<const PackedWeight*> g_registry;
@@ -268,6 +345,7 @@ int il_last_status(void) { return t_last_status; }
 
 int il_get_stats(il_stats* out) {
   if (out == nullptr) return fail(IL_ERR_ARG, "il_get_stats: out is NULL");
+  if (profiling()) drain_times();
   out->uploads = g_stats.uploads.load();
   out->upload_bytes = g_stats.upload_bytes.load();
   out->batches = g_stats.batches.load();
@@ -276,6 +354,8 @@ int il_get_stats(il_stats* out) {
   out->weight_bytes = g_stats.weight_bytes.load();
   out->flops = g_stats.flops.load();
   out->errors = g_stats.errors.load();
+  out->profiled_batches = g_stats.profiled_batches.load();
+  out->device_ns = g_stats.device_ns.load();
   return IL_OK;
 }
 
@@ -288,6 +368,9 @@ void il_reset_stats(void) {
   g_stats.weight_bytes = 0;
   g_stats.flops = 0;
   g_stats.errors = 0;
+  if (profiling()) drain_times();
+  g_stats.profiled_batches = 0;
+  g_stats.device_ns = 0;
 }
 
 }  // extern "C"
@@ -406,11 +489,13 @@ il_weight* upload_impl(const char* fn, int format, const void* const* host, int 
 extern "C" {
 
 il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int64_t n_in) {
+  NvtxRange range("il_upload_weight");
   const void* host[1] = {host_ptr};
   return upload_impl("il_upload_weight", format, host, 1, n_out, n_in);
 }
 
 il_weight* il_upload_gate_up(int format, const void* gate_ptr, const void* up_ptr, int64_t n_out, int64_t n_in) {
+  NvtxRange range("il_upload_gate_up");
   const void* host[2] = {gate_ptr, up_ptr};
   return upload_impl("il_upload_gate_up", format, host, 2, n_out, n_in);
 }
@@ -531,6 +616,7 @@ int il_release_scratch(void* stream_) {
 
 int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
                     void* stream_) {
+  NvtxRange range("il_matmul_batch");
   clear_error();
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   int rc = check_batch_args(x, t, n_in, jobs, n_jobs);
@@ -563,7 +649,7 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
                                 ds->num_sms, ds->status, &launches);
   if (e != cudaSuccess) return cuda_fail(e, "il_matmul_batch: preparing the launches");
   int n_launched = 0;
-  e = run_launches(launches, stream, &n_launched);
+  e = run_timed(launches, stream, &n_launched);
   g_stats.launches.fetch_add((uint64_t)n_launched);
   if (e != cudaSuccess) return cuda_fail(e, "il_matmul_batch: launch");
   g_stats.batches.fetch_add(1);
@@ -576,6 +662,7 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
 int il_centroid_head(const float* x, int64_t h, const il_weight* centroids_h, const il_weight* embed_h,
                      const uint32_t* ordering, int64_t top_k, uint32_t* token_out, float* score_out,
                      uint32_t* selected_out, float* scores_out, void* stream_) {
+  NvtxRange range("il_centroid_head");
   clear_error();
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if (x == nullptr || ordering == nullptr || token_out == nullptr)
@@ -626,7 +713,7 @@ int il_centroid_head(const float* x, int64_t h, const il_weight* centroids_h, co
                        token_out, score_out, ds->status, ds->num_sms, &launches);
   if (e != cudaSuccess) return cuda_fail(e, "il_centroid_head: preparing the launches");
   int n_launched = 0;
-  e = run_launches(launches, stream, &n_launched);
+  e = run_timed(launches, stream, &n_launched);
   g_stats.launches.fetch_add((uint64_t)n_launched);
   if (e != cudaSuccess) return cuda_fail(e, "il_centroid_head: launch");
   g_stats.batches.fetch_add(1);

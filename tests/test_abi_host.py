@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(libil):
 
 def test_version_needs_no_device(libil):
     libil.il_version.restype = ctypes.c_int
-    assert libil.il_version() == 1
+    assert libil.il_version() == 2
 
 
 def test_binding_names_match_abi():
@@ -63,3 +63,18 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(sil, "_lib", None)
     with pytest.raises(sil.ILError):
         sil.load()
+
+
+def test_stats_layout_matches_header(libil):
+    # the binding's il_stats mirror has the header's fields in the header's order,
+    # and il_get_stats fills it without a device (nothing is timed unless IL_PROFILE=1)
+    import shared_input_linear_gb300 as sil
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct \{(.*?)\} il_stats;", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"uint64_t\s+(\w+)\s*;", body)
+    assert [f for f, _ in sil._Stats._fields_] == fields
+    st = sil._Stats()
+    libil.il_get_stats.argtypes = [ctypes.c_void_p]
+    libil.il_get_stats.restype = ctypes.c_int
+    assert libil.il_get_stats(ctypes.byref(st)) == 0

@@ -347,3 +347,40 @@ def test_release_scratch(sil):
             assert oracle.check(y.cpu().numpy(), y_ref, mag)[0]
     for w in ws:
         w.free()
+
+
+_PROFILE_SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r})
+import torch
+torch.cuda.set_device(0)
+import shared_input_linear_gb300 as sil
+import workloads as wl
+b = wl.make_batch(1024, (512, 256), 4, "q8", seed=8)
+ws = [sil.upload_weight(f, buf, n, 1024) for f, buf, n in b.jobs]
+x = torch.from_numpy(b.x).cuda()
+ys = [torch.empty(4, n, device="cuda") for _, _, n in b.jobs]
+sil.reset_stats()
+for _ in range(3):
+    sil.matmul_batch(x, list(zip(ws, ys)))
+st = sil.get_stats()
+print("STATS", st["batches"], st["profiled_batches"], st["device_ns"])
+"""
+
+
+@pytest.mark.parametrize("profile", ["1", "0"])
+def test_profile_timing(profile):
+    # IL_PROFILE=1: every batch is timed with CUDA events and il_get_stats adds the
+    # device time; without it nothing is timed
+    import os
+    env = dict(os.environ, IL_PROFILE=profile)
+    out = subprocess.run([sys.executable, "-c", _PROFILE_SCRIPT.format(root=ROOT)], capture_output=True,
+                         text=True, timeout=300, env=env)
+    line = [l for l in out.stdout.splitlines() if l.startswith("STATS")]
+    assert line, out.stdout + out.stderr
+    batches, profiled, ns = (int(v) for v in line[0].split()[1:])
+    assert batches == 3
+    if profile == "1":
+        assert profiled == 3 and 0 < ns < 3_000_000_000
+    else:
+        assert profiled == 0 and ns == 0
