@@ -146,10 +146,13 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
  *     process exits.  A batch needing more, t * round_up(n_in, 256) * 2 bytes
  *     > 16 MiB, is rejected with IL_ERR_UNSUPPORTED (e.g. t = 2048 fits at
  *     n_in = 4096, not at 12288).
- *   - The first call on a device looks up the array's device address and
- *     clears the library's status word there, asynchronously on `stream`; make
+ *   - The Q8/Q4 decode kernel's partial sums of tiles whose K it splits over
+ *     CTAs go to a fixed 4 MiB device array (with their arrival counters); a
+ *     batch whose plan would need more splits K less.
+ *   - The first call on a device looks up the arrays' device addresses and
+ *     clears the library's status word and counters there, asynchronously on `stream`; make
  *     that first call before any stream capture.
- *   - Every call shares the one array: calls that overlap on the GPU (on
+ *   - Every call shares the same arrays: calls that overlap on the GPU (on
  *     different streams, or from different threads) race and may corrupt each
  *     other's results.  Serialise them, e.g. on one stream.
  *   - A device-side wait that gives up records its code in that status word
