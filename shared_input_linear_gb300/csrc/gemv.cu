@@ -8,7 +8,9 @@
 //  * One launch covers every job: rows of all jobs are cut into groups of 8
 //    and the groups are concatenated; a row block is 8 warps x G groups.
 //  * Each weight byte is streamed from HBM exactly once, as 16-byte loads per
-//    lane, prefetched P chunks ahead in registers.
+//    lane, two batches of 4 chunks in flight in registers; before the launch
+//    waits for the previous kernel, up to three more batches per warp are
+//    copied into shared memory (cp.async) so HBM stays busy across the hand-off.
 //  * The per-(row, token) dot products run on the tensor cores with
 //    mma.m16n8k16 (bf16 in, fp32 accumulate): the weight is the 16x8 "B"
 //    operand (8 rows), and the "A" operand holds 8 tokens of x split into a
@@ -25,9 +27,8 @@
 #include <cooperative_groups.h>
 
 #include <algorithm>
-
-#include <mutex>
 #include <map>
+#include <mutex>
 #include <tuple>
 
 #include "il_internal.cuh"
