@@ -16,11 +16,14 @@
 // Warp roles (6 warps): 0 = TMA producer, 1 = TMEM allocator + MMA issuer,
 // 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
 //
-// Q8 / Q4 weights (a mixed-input GEMM, 10 warps): the producer brings the packed
+// Q8 / Q4 weights (a mixed-input GEMM, 22 warps): the producer brings the packed
 // quants and scales of 16 row groups (128 rows) x one chunk by TMA into a ring of
-// raw stages; warps 6..9 turn them into the bf16 A tile of a pipeline stage,
+// raw stages; warps 6..21 turn them into the bf16 A tile of a pipeline stage,
 // bf16(fp32(d*q)) with round to nearest even, written in the 128-byte swizzle
 // the MMA reads.  The weight crosses HBM once, in its packed form.
+// Tiles are taken round-robin by persistent CTAs; when the tiles cannot fill the
+// SMs, each is split over K in two and the slice that arrives last adds both
+// partial tiles (from a global workspace) in slice order.
 // Every mbarrier wait is bounded; a wait that gives up records an error code
 // in the device status word, raises a CTA-wide abort flag and lets every role
 // leave its loop; TMEM is always released before exit.

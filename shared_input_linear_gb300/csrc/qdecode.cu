@@ -10,9 +10,11 @@
 //    (tile, chunk) of a packed Q8/Q4 weight is one contiguous record of quants and
 //    scales (il_internal.cuh).  Each weight byte crosses HBM once.
 //  * The records stream into shared memory by bulk copies (cp.async.bulk,
-//    completion counted on an mbarrier).  Every warp owns a ring of stages, one
-//    record each, and refills a stage as soon as it has consumed it, so the bytes
-//    in flight per SM are set by the ring depth, not by registers.
+//    completion counted on an mbarrier).  Every warp owns a ring of stages of up
+//    to four consecutive records of one tile (one copy each) and refills a stage
+//    as soon as it has consumed it, so the bytes in flight per SM are set by the
+//    ring depth, not by registers; the first stages are issued before the launch
+//    waits for the previous kernel.
 //  * Dot products run on the tensor cores (mma.m16n8k16, fp16 in, fp32
 //    accumulate).  The 16 weight rows of a record are the A operand, decoded in
 //    registers to exact fp16 integers (one byte permute or LOP3 and one fp16x2
@@ -21,9 +23,10 @@
 //    22 significant bits), for t <= 8 the fp16 value (11 bits); one MMA per 16
 //    columns of K either way.  The fp32 scale of each 32-block multiplies the
 //    fp32 partial of that block.
-//  * x is staged once per CTA in shared memory, already as B fragments, only for
-//    the lanes whose token exists (4 t bytes per column), scaled per token by a
-//    power of two so that fp16 holds it (undone on the partial sums).
+//  * x is staged once per CTA in shared memory, already as B fragments (zeros for
+//    tokens >= t), scaled per token by a power of two so that fp16 holds it
+//    (undone on the partial sums); the loads, the token maxima and the conversion
+//    take one pass over L2 from registers.
 //  * Work: the CTAs of a K split of C take the same tiles with different K
 //    slices; inside a CTA, warps stand in a grid of wr row tiles x wk parts of
 //    the slice (wk = 1: a warp owns whole tiles).  There is no CTA-wide barrier
