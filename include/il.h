@@ -113,13 +113,12 @@ il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int
  * "launch") can leave the earlier launches of the batch enqueued.  On success
  * the work is enqueued asynchronously on `stream`; x, y and the handles must
  * stay valid until it completes.
- * Kernels: small t runs the grouped decode kernel, each weight byte streamed
- * once per 8 tokens: t <= 8 for bf16 weights, t <= 16 for Q8/Q4.  Larger t casts
- * x to bf16 once and runs the tensor-core kernel (Q8/Q4 weights dequantised to
- * bf16 in shared memory, bf16(fp32(d*q))).  One launch covers every job of one
- * format, up to 32 jobs on the decode kernel (per 8 tokens) and 8 jobs on the
- * tensor-core kernel; a batch beyond those counts, or with several formats,
- * takes one launch per group.
+ * Kernels: small t runs the grouped decode kernels, each weight byte streamed
+ * once: t <= 8 for bf16 weights, t <= 16 for Q8/Q4.  Larger t casts x to bf16
+ * once and runs the tensor-core kernel (Q8/Q4 weights dequantised to bf16 in
+ * shared memory, bf16(fp32(d*q))).  One launch covers every job of one format,
+ * up to 32 jobs on a decode kernel and 8 jobs on the tensor-core kernel; a batch
+ * beyond those counts, or with several formats, takes one launch per group.
  * Scratch: the tensor-core path keeps a bf16 copy of x and a split-K workspace
  * per (device, stream), owned by the library.  They grow with the stream-ordered
  * allocator (cudaMallocAsync / cudaFreeAsync on `stream`), so growing never

@@ -771,18 +771,19 @@ void plan_batch(int64_t t, const il_job* jobs, int n_jobs, const std::vector<con
 namespace {
 
 // The decode launches of a plan, in launch order: one per format, per
-// kMaxDecodeJobs jobs and per 8 tokens.
+// kMaxDecodeJobs jobs and per 8 tokens (bf16) or 16 tokens (Q8/Q4).
 void decode_launch_params(const BatchPlan& plan, const float* x, int64_t t, int64_t n_in, const il_job* jobs,
                           const std::vector<const PackedWeight*>& ws, std::vector<std::pair<int, DecodeParams>>* out) {
   for (int fmt = IL_BF16; fmt <= IL_Q4; ++fmt) {
     const std::vector<int>& idx = plan.decode[fmt];
     for (size_t j0 = 0; j0 < idx.size(); j0 += kMaxDecodeJobs) {
       const size_t j1 = std::min(idx.size(), j0 + (size_t)kMaxDecodeJobs);
-      for (int64_t t0 = 0; t0 < t; t0 += 8) {
+      const int64_t tokens = fmt == IL_BF16 ? kDecodeTokensBf16 : kDecodeTokensQ;
+      for (int64_t t0 = 0; t0 < t; t0 += tokens) {
         DecodeParams p;
         memset(&p, 0, sizeof p);
         p.x = x != nullptr ? x + t0 * n_in : nullptr;
-        p.t = (int)std::min<int64_t>(8, t - t0);
+        p.t = (int)std::min<int64_t>(tokens, t - t0);
         p.x_row_stride = (int)n_in;
         p.n_in = (int)n_in;
         int groups = 0;

@@ -244,7 +244,12 @@ cudaError_t run_launches(const std::vector<Launch>& v, cudaStream_t stream, int*
 // Upload-time repack and the dequantise hook: single launches, enqueued directly.
 cudaError_t launch_pack(const PackedWeight& w, const uint8_t* staging, cudaStream_t stream);
 cudaError_t launch_dequant(const PackedWeight& w, float* out, cudaStream_t stream);
-// Decode kernel for t <= 8 tokens: bf16 weights run the register-streaming kernel
+// Tokens of one decode launch: bf16 weights 8 (the MMA's 8 columns), Q8/Q4 16 (two
+// groups of 8 columns fed by the same decoded weights).
+constexpr int kDecodeTokensBf16 = 8;
+constexpr int kDecodeTokensQ = 16;
+
+// Decode kernel for one launch of tokens (see above): bf16 weights run the register-streaming kernel
 // (gemv.cu), Q8 / Q4 weights the shared-memory ring kernel (qdecode.cu), whose
 // bounded waits record a code in `status` when they give up.
 cudaError_t prepare_decode(int fmt, const DecodeParams& p, int num_sms, unsigned* status, void* ws,
@@ -260,7 +265,7 @@ cudaError_t prepare_cast_bf16(const float* x, int64_t t, int64_t n_in, int64_t n
                               int num_sms, Launch* L);
 
 // Token counts from which a batch takes the tensor-core path instead of the
-// decode kernel (which streams the weights once per 8 tokens).
+// decode kernels (which stream the weights once per launch of tokens).
 constexpr int64_t kGemmMinT = 9;        // bf16 weights
 constexpr int64_t kGemmMinTQuant = 17;  // Q8 / Q4 weights
 

@@ -419,6 +419,19 @@ def test_twelve_gemm_jobs_two_launches(sil):
     assert_parity(b, ys, "12 GEMM jobs")
 
 
+@pytest.mark.parametrize("fmt", ["q8", "q4"])
+@pytest.mark.parametrize("t", [9, 12, 16])
+def test_quant_decode_sixteen_tokens_one_launch(sil, fmt, t):
+    # Q8/Q4 at 9 <= t <= 16: one decode launch streams each weight once for two
+    # groups of 8 token columns; ragged rows and a K split over CTAs (n_in 12288)
+    for n_in, n_outs in ((1024, (300, 72)), (12288, (136,))):
+        b = wl.make_batch(n_in, n_outs, t, fmt, seed=t + n_in)
+        ys, guards, launches = _launches(sil, b)
+        assert guards
+        assert launches == 1
+        assert_parity(b, ys, f"{fmt} t={t}")
+
+
 def test_forty_decode_jobs_two_launches(sil):
     # 40 bf16 jobs at t = 1: 32 + 8 jobs on the decode kernel
     n_outs = tuple(8 + 16 * (j % 7) for j in range(40))
