@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define IL_VERSION 2
+#define IL_VERSION 3
 
 /* Storage format of a weight (oxinfer src/gpu.rs, enum WeightRef). */
 typedef enum { IL_BF16 = 0, IL_Q8 = 1, IL_Q4 = 2 } il_format;
@@ -58,9 +58,9 @@ typedef struct il_weight il_weight;
 /* One job of a batch (the page's `Job`): y[t][n_out] = x[t][n_in] * W^T.
  *   w     : handle from il_upload_weight; its n_in must equal the batch n_in.
  *   n_out : must equal the handle's n_out.
- *   y     : DEVICE pointer, fp32 [t][n_out] row-major, 4-byte aligned; it is
- *           overwritten (not accumulated) and must not overlap x or any other
- *           job's y. */
+ *   y     : DEVICE pointer (HOST pointer for il_matmul_batch_host), fp32
+ *           [t][n_out] row-major, 4-byte aligned; it is overwritten (not
+ *           accumulated) and must not overlap x or any other job's y. */
 typedef struct {
   const il_weight* w;
   int64_t n_out;
@@ -71,7 +71,7 @@ typedef struct {
 typedef struct {
   uint64_t uploads;           /* successful il_upload_weight calls        */
   uint64_t upload_bytes;      /* host bytes uploaded (WeightRef::bytes)   */
-  uint64_t batches;           /* successful il_matmul_batch calls         */
+  uint64_t batches;           /* successful il_matmul_batch* calls        */
   uint64_t jobs;              /* jobs in those batches                    */
   uint64_t launches;          /* kernels launched by those batches        */
   uint64_t weight_bytes;      /* weight bytes those batches streamed      */
@@ -128,6 +128,38 @@ il_weight* il_upload_weight(int format, const void* host_ptr, int64_t n_out, int
  */
 int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
                     void* stream);
+
+/*
+ * il_matmul_batch_host -- il_matmul_batch on HOST buffers, the form in which
+ * the pages' `Backend::matmul` takes them (oxinfer src/gpu.rs: `x: &[f32]`,
+ * and each `Job` holds `y: &mut [f32]`).
+ *   x      : HOST pointer, fp32 [t][n_in] row-major (any alignment).
+ *   jobs   : as for il_matmul_batch, but every y is a HOST pointer, fp32
+ *            [t][n_out] row-major, 4-byte aligned, overwritten.
+ *   t, n_in, n_jobs, stream : as for il_matmul_batch.
+ * Host memory may be page-locked (cudaHostAlloc, cudaHostRegister, a pinned
+ * torch tensor), pageable or managed; a device pointer for x or a y is
+ * rejected with IL_ERR_ARG.  Page-locked buffers are used in place: the kernels
+ * read x and write y through their mapped device addresses (over NVLink-C2C on
+ * GB300), with no copy operation (a page-locked x that is not 16-byte aligned is
+ * copied as below).  Other buffers go through a library-owned device buffer:
+ * one copy of x in before the launches, and after them one device->host copy
+ * per run of y buffers (y buffers that follow one another in host memory, each
+ * starting where the previous one ends, come back in one copy).  Everything is
+ * enqueued on `stream` and the call returns once it is; y holds the results
+ * after `stream` has completed that work (e.g. cudaStreamSynchronize), and x and
+ * y must stay valid, x unchanged, until then.  With page-locked memory nothing
+ * blocks the calling thread; with pageable memory the copies behave as
+ * cudaMemcpyAsync does for it (the copy of y waits for the kernels).
+ * Validation and launch preparation happen before anything is enqueued, with
+ * the same rule as il_matmul_batch: an error returns a negative il_status with
+ * nothing enqueued, except a copy or launch that the CUDA runtime itself
+ * rejects (IL_ERR_CUDA) after earlier work of the call was enqueued.  The
+ * device buffer of x and y is scratch per (device, stream), grown and freed
+ * like the bf16 copy of x (not during stream capture; il_release_scratch).
+ */
+int il_matmul_batch_host(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
+                         void* stream);
 
 /*
  * il_matmul_batch_noalloc -- the pages have no counterpart of this entry point.
@@ -259,7 +291,8 @@ int il_dequantize_weight(const il_weight* w, float* dev_out, void* stream);
 int il_check_device_status(void* stream);
 
 /* Frees the scratch the library keeps for `stream` on the current device (the
- * bf16 copy of x, the split-K workspace, the LM-head scratch), in stream order:
+ * bf16 copy of x, the split-K workspace, the LM-head scratch, the device copies
+ * of x and y of il_matmul_batch_host), in stream order:
  * call it before destroying a stream the library has run on.  A later call on
  * the stream allocates afresh.  Returns IL_OK or IL_ERR_CUDA. */
 int il_release_scratch(void* stream);

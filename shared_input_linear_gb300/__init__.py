@@ -77,6 +77,8 @@ def load() -> ctypes.CDLL:
         lib.il_matmul_batch.restype = ci
         lib.il_matmul_batch_noalloc.argtypes = [vp, i64, i64, ctypes.POINTER(_Job), ci, vp]
         lib.il_matmul_batch_noalloc.restype = ci
+        lib.il_matmul_batch_host.argtypes = [vp, i64, i64, ctypes.POINTER(_Job), ci, vp]
+        lib.il_matmul_batch_host.restype = ci
         lib.il_upload_gate_up.argtypes = [ci, vp, vp, i64, i64]
         lib.il_upload_gate_up.restype = vp
         lib.il_centroid_head.argtypes = [vp, i64, vp, vp, vp, i64, vp, vp, vp, vp, vp]
@@ -268,6 +270,44 @@ def matmul_batch(x, jobs, stream=None) -> None:
             raise ILError(-1, "y must be contiguous")
         lst.append((w, w.n_out, y.data_ptr()))
     matmul_batch_ptr(x.data_ptr(), t, n_in, lst, _stream_ptr(stream))
+
+
+def matmul_batch_host_prepared(x_ptr: int, t: int, n_in: int, prepared, stream_ptr: int) -> int:
+    """``il_matmul_batch_host`` with a job array from :func:`prepare_jobs` whose y
+    pointers are host addresses; ``x_ptr`` is a host address too."""
+    arr, n = prepared
+    return _check(load().il_matmul_batch_host(x_ptr, int(t), int(n_in), arr, n, stream_ptr))
+
+
+def matmul_batch_host(x, jobs, stream=None, sync: bool = True) -> None:
+    """``il_matmul_batch_host`` on CPU torch tensors (pinned or not).
+
+    ``x``: fp32 ``[t][n_in]`` contiguous; ``jobs``: ``[(Weight, y)]`` with ``y``
+    fp32 ``[t][n_out]`` contiguous on the CPU, overwritten.  Enqueued on
+    ``stream`` (default: the current torch stream); with ``sync`` the call waits
+    for the stream, so ``y`` holds the results when it returns.
+    """
+    if x.device.type != "cpu" or x.dim() != 2 or not x.is_contiguous():
+        raise ILError(-1, "x must be a contiguous [t][n_in] CPU tensor")
+    t, n_in = x.shape
+    lst = []
+    for w, y in jobs:
+        if y.device.type != "cpu" or not y.is_contiguous():
+            raise ILError(-1, "y must be a contiguous CPU tensor")
+        lst.append((w, w.n_out, y.data_ptr()))
+    sp = _stream_ptr(stream)
+    arr = (_Job * max(1, len(lst)))()
+    for i, (w, n_out, y) in enumerate(lst):
+        arr[i].w = w.handle if isinstance(w, Weight) else w
+        arr[i].n_out = int(n_out)
+        arr[i].y = int(y)
+    _check(load().il_matmul_batch_host(x.data_ptr(), int(t), int(n_in), arr, len(lst), sp))
+    if sync:
+        import torch
+        if sp:
+            torch.cuda.ExternalStream(sp).synchronize()
+        else:
+            torch.cuda.synchronize()
 
 
 def dequantize_weight(w: Weight, out, stream=None) -> None:

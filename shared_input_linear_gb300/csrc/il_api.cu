@@ -331,7 +331,85 @@ int get_head_scratch(int dev, cudaStream_t stream, int64_t n_cent, int64_t k, ui
   return IL_OK;
 }
 
+// Device copies of x and y for il_matmul_batch_host, one buffer per (device,
+// stream): x at the start, then the y runs.  Grown like the bf16 copy of x.
+struct HostStaging {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, HostStaging> g_host_staging;
+
+int get_host_staging(int dev, cudaStream_t stream, size_t bytes, uint8_t** out) {
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  HostStaging& s = g_host_staging[{dev, stream}];
+  if (s.bytes < bytes) {
+    const int rc = check_not_capturing(stream, "the device copies of x and y");
+    if (rc != IL_OK) return rc;
+    const size_t want = bytes + bytes / 4;
+    void* np = nullptr;
+    cudaError_t e = il_malloc_async(&np, want, stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(IL_ERR_OOM, "allocating %zu bytes for the device copies of x and y failed", want);
+    }
+    if (s.ptr != nullptr) cudaFreeAsync(s.ptr, stream);
+    s.ptr = np;
+    s.bytes = want;
+  }
+  *out = static_cast<uint8_t*>(s.ptr);
+  return IL_OK;
+}
+
+// A buffer of il_matmul_batch_host must be host memory (page-locked or pageable)
+// or managed memory; device memory is il_matmul_batch's.  *mapped: the device
+// address of page-locked host memory that kernels can access in place (NULL for
+// pageable or managed memory).
+int host_buffer(const void* ptr, const char* what, int job, void** mapped) {
+  *mapped = nullptr;
+  cudaPointerAttributes a;
+  const cudaError_t e = cudaPointerGetAttributes(&a, ptr);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "il_matmul_batch_host: cudaPointerGetAttributes");
+  }
+  if (a.type == cudaMemoryTypeDevice) {
+    if (job < 0) return fail(IL_ERR_ARG, "il_matmul_batch_host: %s is device memory (use il_matmul_batch)", what);
+    return fail(IL_ERR_ARG, "il_matmul_batch_host: job %d %s is device memory (use il_matmul_batch)", job, what);
+  }
+  if (a.type == cudaMemoryTypeHost) *mapped = a.devicePointer;
+  return IL_OK;
+}
+
 bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+// Plan, scratch and every launch of a validated batch on device buffers, all
+// worked out before anything is enqueued.
+int prepare_device_batch(const char* fn, const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
+                         const std::vector<const PackedWeight*>& ws, int dev, DeviceState* ds, cudaStream_t stream,
+                         std::vector<Launch>* launches) {
+  BatchPlan plan;
+  plan_batch(t, jobs, n_jobs, ws, /*gemm_quant=*/true, &plan);
+  void* xb = nullptr;
+  void* wsp = nullptr;
+  size_t ws_bytes = 0;
+  if (plan.xb_bytes > 0) {
+    const int rc = get_scratch(dev, stream, plan.xb_bytes, &xb);
+    if (rc != IL_OK) return rc;
+  }
+  const size_t want = plan_workspace_bytes(plan, t, n_in, jobs, ws, ds->num_sms);
+  if (want > 0) {
+    const int rc = get_workspace(dev, stream, want, &wsp, &ws_bytes);
+    if (rc != IL_OK) return rc;
+  }
+  const cudaError_t e = prepare_batch(plan, x, t, n_in, jobs, ws, static_cast<__nv_bfloat16*>(xb), wsp, ws_bytes,
+                                      ds->num_sms, ds->status, launches);
+  if (e != cudaSuccess) {
+    char what[96];
+    snprintf(what, sizeof what, "%s: preparing the launches", fn);
+    return cuda_fail(e, what);
+  }
+  return IL_OK;
+}
 
 }  // namespace
 
@@ -610,6 +688,11 @@ int il_release_scratch(void* stream_) {
     if (e == cudaSuccess && ih->second.ptr != nullptr) e = cudaFreeAsync(ih->second.ptr, stream);
     g_head_scratch.erase(ih);
   }
+  auto is = g_host_staging.find({dev, stream});
+  if (is != g_host_staging.end()) {
+    if (e == cudaSuccess && is->second.ptr != nullptr) e = cudaFreeAsync(is->second.ptr, stream);
+    g_host_staging.erase(is);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "il_release_scratch");
   return IL_OK;
 }
@@ -628,30 +711,103 @@ int il_matmul_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs,
   uint64_t wbytes = 0, flops = 0;
   rc = api_check_batch(x, t, n_in, jobs, n_jobs, dev, &ws, &wbytes, &flops);
   if (rc != IL_OK) return rc;
-
-  // ---- plan, scratch, and every launch prepared before the first is enqueued
-  BatchPlan plan;
-  plan_batch(t, jobs, n_jobs, ws, /*gemm_quant=*/true, &plan);
-  void* xb = nullptr;
-  void* wsp = nullptr;
-  size_t ws_bytes = 0;
-  if (plan.xb_bytes > 0) {
-    rc = get_scratch(dev, stream, plan.xb_bytes, &xb);
-    if (rc != IL_OK) return rc;
-  }
-  const size_t want = plan_workspace_bytes(plan, t, n_in, jobs, ws, ds->num_sms);
-  if (want > 0) {
-    rc = get_workspace(dev, stream, want, &wsp, &ws_bytes);
-    if (rc != IL_OK) return rc;
-  }
   std::vector<Launch> launches;
-  cudaError_t e = prepare_batch(plan, x, t, n_in, jobs, ws, static_cast<__nv_bfloat16*>(xb), wsp, ws_bytes,
-                                ds->num_sms, ds->status, &launches);
-  if (e != cudaSuccess) return cuda_fail(e, "il_matmul_batch: preparing the launches");
+  rc = prepare_device_batch("il_matmul_batch", x, t, n_in, jobs, n_jobs, ws, dev, ds, stream, &launches);
+  if (rc != IL_OK) return rc;
+  int n_launched = 0;
+  const cudaError_t e = run_timed(launches, stream, &n_launched);
+  g_stats.launches.fetch_add((uint64_t)n_launched);
+  if (e != cudaSuccess) return cuda_fail(e, "il_matmul_batch: launch");
+  g_stats.batches.fetch_add(1);
+  g_stats.jobs.fetch_add((uint64_t)n_jobs);
+  g_stats.weight_bytes.fetch_add(wbytes);
+  g_stats.flops.fetch_add(flops);
+  return IL_OK;
+}
+
+int il_matmul_batch_host(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs,
+                         void* stream_) {
+  NvtxRange range("il_matmul_batch_host");
+  clear_error();
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int rc = check_batch_args(x, t, n_in, jobs, n_jobs, /*host_x=*/true);
+  if (rc != IL_OK || t == 0 || n_jobs == 0) return rc;
+  DeviceState* ds = nullptr;
+  const int dev = current_device(&ds);
+  if (dev < 0) return dev;
+  std::vector<const PackedWeight*> ws;
+  uint64_t wbytes = 0, flops = 0;
+  rc = api_check_batch(x, t, n_in, jobs, n_jobs, dev, &ws, &wbytes, &flops, /*host_x=*/true);
+  if (rc != IL_OK) return rc;
+  // page-locked host memory is read (x, when 16-byte aligned) and written (y) by
+  // the kernels in place; the rest goes through a device buffer and copies
+  void* x_mapped = nullptr;
+  rc = host_buffer(x, "x", -1, &x_mapped);
+  if (rc != IL_OK) return rc;
+  if (reinterpret_cast<uintptr_t>(x_mapped) % 16 != 0) x_mapped = nullptr;
+  std::vector<void*> y_mapped(n_jobs, nullptr);
+  for (int j = 0; j < n_jobs && rc == IL_OK; ++j) rc = host_buffer(jobs[j].y, "y", j, &y_mapped[j]);
+  if (rc != IL_OK) return rc;
+
+  // ---- device buffer: x (if copied) at offset 0, then the copied y buffers in
+  // runs -- a run is a sequence of y buffers each starting where the previous one
+  // ends in host memory, kept adjacent on the device too so that one copy brings
+  // it back
+  struct Run {
+    uintptr_t host;
+    size_t bytes, dev_off;
+  };
+  auto round_up = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
+  const size_t x_bytes = (size_t)t * (size_t)n_in * sizeof(float);
+  std::vector<int> order;
+  for (int j = 0; j < n_jobs; ++j)
+    if (y_mapped[j] == nullptr) order.push_back(j);
+  std::sort(order.begin(), order.end(), [&](int a, int b) {
+    return reinterpret_cast<uintptr_t>(jobs[a].y) < reinterpret_cast<uintptr_t>(jobs[b].y);
+  });
+  std::vector<Run> runs;
+  std::vector<size_t> y_off(n_jobs, 0);
+  size_t end = x_mapped == nullptr ? round_up(x_bytes, 256) : 0;
+  for (int j : order) {
+    const uintptr_t y0 = reinterpret_cast<uintptr_t>(jobs[j].y);
+    const size_t yb = (size_t)t * (size_t)jobs[j].n_out * sizeof(float);
+    if (!runs.empty() && runs.back().host + runs.back().bytes == y0) {
+      runs.back().bytes += yb;
+    } else {
+      runs.push_back(Run{y0, yb, round_up(end, 256)});
+    }
+    y_off[j] = runs.back().dev_off + (size_t)(y0 - runs.back().host);
+    end = runs.back().dev_off + runs.back().bytes;
+  }
+  uint8_t* staging = nullptr;
+  if (end > 0) {
+    rc = get_host_staging(dev, stream, end, &staging);
+    if (rc != IL_OK) return rc;
+  }
+  std::vector<il_job> djobs(jobs, jobs + n_jobs);
+  for (int j = 0; j < n_jobs; ++j)
+    djobs[j].y = y_mapped[j] != nullptr ? static_cast<float*>(y_mapped[j])
+                                        : reinterpret_cast<float*>(staging + y_off[j]);
+  const float* xd = x_mapped != nullptr ? static_cast<const float*>(x_mapped) : reinterpret_cast<const float*>(staging);
+  std::vector<Launch> launches;
+  rc = prepare_device_batch("il_matmul_batch_host", xd, t, n_in, djobs.data(), n_jobs, ws, dev, ds, stream,
+                            &launches);
+  if (rc != IL_OK) return rc;
+
+  // ---- enqueue: x in (if copied), the launches, every run out
+  cudaError_t e = cudaSuccess;
+  if (x_mapped == nullptr) {
+    e = cudaMemcpyAsync(staging, x, x_bytes, cudaMemcpyDefault, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "il_matmul_batch_host: copying x to the device");
+  }
   int n_launched = 0;
   e = run_timed(launches, stream, &n_launched);
   g_stats.launches.fetch_add((uint64_t)n_launched);
-  if (e != cudaSuccess) return cuda_fail(e, "il_matmul_batch: launch");
+  if (e != cudaSuccess) return cuda_fail(e, "il_matmul_batch_host: launch");
+  for (const Run& r : runs) {
+    e = cudaMemcpyAsync(reinterpret_cast<void*>(r.host), staging + r.dev_off, r.bytes, cudaMemcpyDefault, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "il_matmul_batch_host: copying y to the host");
+  }
   g_stats.batches.fetch_add(1);
   g_stats.jobs.fetch_add((uint64_t)n_jobs);
   g_stats.weight_bytes.fetch_add(wbytes);
@@ -858,14 +1014,14 @@ int api_fail(int code, const char* msg) { return fail(code, "%s", msg); }
 
 int api_cuda_fail(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 
-// The checks that need no device: sizes, null pointers, x alignment.
-int check_batch_args(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs) {
+// The checks that need no device: sizes, null pointers, x alignment (device x).
+int check_batch_args(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs, bool host_x) {
   if (t < 0 || t > kMaxT) return fail(IL_ERR_ARG, "t=%lld out of range", (long long)t);
   if (n_jobs < 0 || n_jobs > kMaxJobs) return fail(IL_ERR_ARG, "n_jobs=%d out of range", n_jobs);
   if (t == 0 || n_jobs == 0) return IL_OK;
   if (x == nullptr) return fail(IL_ERR_ARG, "x is NULL");
   if (jobs == nullptr) return fail(IL_ERR_ARG, "jobs is NULL");
-  if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return fail(IL_ERR_ARG, "x is not 16-byte aligned");
+  if (!host_x && reinterpret_cast<uintptr_t>(x) % 16 != 0) return fail(IL_ERR_ARG, "x is not 16-byte aligned");
   if (n_in < 1 || n_in > kMaxNIn) return fail(IL_ERR_SHAPE, "n_in=%lld out of range", (long long)n_in);
   return IL_OK;
 }
@@ -873,11 +1029,11 @@ int check_batch_args(const float* x, int64_t t, int64_t n_in, const il_job* jobs
 // Every job's checks on the calling thread's device `dev`; on success fills `ws`
 // with the weight of each job.
 int api_check_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs, int dev,
-                    std::vector<const PackedWeight*>* ws, uint64_t* wbytes, uint64_t* flops) {
+                    std::vector<const PackedWeight*>* ws, uint64_t* wbytes, uint64_t* flops, bool host_x) {
   ws->clear();
   *wbytes = 0;
   *flops = 0;
-  int rc = check_batch_args(x, t, n_in, jobs, n_jobs);
+  int rc = check_batch_args(x, t, n_in, jobs, n_jobs, host_x);
   if (rc != IL_OK || t == 0 || n_jobs == 0) return rc;
   std::vector<std::pair<uintptr_t, uintptr_t>> ranges;
   ranges.reserve(n_jobs + 1);

@@ -314,9 +314,10 @@ cudaError_t prepare_batch(const BatchPlan& plan, const float* x, int64_t t, int6
                           size_t ws_bytes, int num_sms, unsigned* status, std::vector<Launch>* out);
 
 // Argument checks shared by the batch entry points (set the thread's error on failure).
-int check_batch_args(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs);
+// host_x: x is a host buffer that the call copies (no alignment rule for it).
+int check_batch_args(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs, bool host_x = false);
 int api_check_batch(const float* x, int64_t t, int64_t n_in, const il_job* jobs, int n_jobs, int dev,
-                    std::vector<const PackedWeight*>* ws, uint64_t* wbytes, uint64_t* flops);
+                    std::vector<const PackedWeight*>* ws, uint64_t* wbytes, uint64_t* flops, bool host_x = false);
 void api_clear_error();
 int api_fail(int code, const char* msg);
 int api_cuda_fail(cudaError_t e, const char* what);

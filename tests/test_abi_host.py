@@ -38,12 +38,12 @@ def test_every_declared_symbol_is_exported(libil):
 
 def test_version_needs_no_device(libil):
     libil.il_version.restype = ctypes.c_int
-    assert libil.il_version() == 2
+    assert libil.il_version() == 3
 
 
 def test_binding_names_match_abi():
     import shared_input_linear_gb300 as sil
-    for name in ("upload_weight", "matmul_batch", "free_weight", "weight_bytes",
+    for name in ("upload_weight", "matmul_batch", "matmul_batch_host", "free_weight", "weight_bytes",
                  "dequantize_weight", "get_stats", "last_error", "check_device_status"):
         assert callable(getattr(sil, name))
 
@@ -78,3 +78,25 @@ def test_stats_layout_matches_header(libil):
     libil.il_get_stats.argtypes = [ctypes.c_void_p]
     libil.il_get_stats.restype = ctypes.c_int
     assert libil.il_get_stats(ctypes.byref(st)) == 0
+
+
+def test_host_entry_checks_arguments_before_the_device(libil):
+    # il_matmul_batch_host: sizes and NULL pointers are refused before any device
+    # is touched, and t == 0 / n_jobs == 0 are successful no-ops (as il_matmul_batch)
+    f = libil.il_matmul_batch_host
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int,
+                  ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    job = (ctypes.c_char * 24)()
+    x = (ctypes.c_float * 8)()
+    assert f(None, 0, 8, None, 0, None) == 0
+    assert f(ctypes.addressof(x), 1, 8, ctypes.addressof(job), 0, None) == 0
+    assert f(None, 1, 8, ctypes.addressof(job), 1, None) == -1        # IL_ERR_ARG: x is NULL
+    assert f(ctypes.addressof(x), -1, 8, ctypes.addressof(job), 1, None) == -1
+    assert f(ctypes.addressof(x), 1, 8, None, 1, None) == -1          # jobs is NULL
+    assert f(ctypes.addressof(x), 1, 0, ctypes.addressof(job), 1, None) == -2   # IL_ERR_SHAPE: n_in
+    # a host x needs no 16-byte alignment (it is copied): an odd address passes
+    # the argument checks and fails later, at the first device step, not with IL_ERR_ARG
+    libil.il_last_error.restype = ctypes.c_char_p
+    rc = f(ctypes.addressof(x) + 4, 1, 8, None, 1, None)
+    assert rc == -1 and b"jobs" in libil.il_last_error()
