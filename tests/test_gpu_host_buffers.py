@@ -186,3 +186,37 @@ def test_graph_capture_with_pinned_buffers():
     finally:
         for w in ws:
             w.free()
+
+
+@pytest.mark.parametrize("t", [1, 12, 40])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_mixed_formats_and_fused_gate_up_on_host_buffers(t, pinned):
+    # a fused gate+up job next to plain jobs of every format, over one host x:
+    # one launch per format, every y back in host memory
+    import oracle
+    import torch
+    sil = lib()
+    n_in = 512
+    gu = wl.make_batch(n_in, (200, 200), t, "q8", seed=60 + t)
+    x, gate, up = gu.x, gu.jobs[0][1], gu.jobs[1][1]
+    fused = sil.upload_gate_up("q8", gate, up, 200, n_in)
+    plain = [wl.make_batch(n_in, (n,), 1, f, seed=70 + i).jobs[0] for i, (f, n) in
+             enumerate((("bf16", 96), ("q4", 64), ("q8", 40)))]
+    pw = [sil.upload_weight(f, buf, n, n_in) for f, buf, n in plain]
+    try:
+        widths = [200] + [n for _, _, n in plain]
+        bufs = [torch.full((2 * GUARD + t * n,), float("nan"), pin_memory=pinned) for n in widths]
+        ys = [b[GUARD:GUARD + t * n].view(t, n) for b, n in zip(bufs, widths)]
+        sil.matmul_batch_host(torch.from_numpy(x), list(zip([fused] + pw, ys)))
+        for b, n in zip(bufs, widths):
+            h = b.numpy()
+            assert np.all(np.isnan(np.concatenate([h[:GUARD], h[GUARD + t * n:]])))
+        h_ref, g, u, mg, mu = oracle.gate_up("q8", gate, up, 200, n_in, x)
+        assert oracle.check_gate_up(ys[0].numpy(), g, u, mg, mu)[0]
+        for (f, buf, n), y in zip(plain, ys[1:]):
+            y_ref, mag = oracle.linear(f, buf, n, n_in, x)
+            assert oracle.check(y.numpy(), y_ref, mag)[0], f
+    finally:
+        fused.free()
+        for w in pw:
+            w.free()
