@@ -22,17 +22,23 @@
 // bf16(fp32(d*q)) with round to nearest even, written in the 128-byte swizzle
 // the MMA reads.  The weight crosses HBM once, in its packed form.
 // Tiles are taken round-robin by persistent CTAs; when the tiles cannot fill the
-// SMs, each is split over K in two and the slice that arrives last adds both
-// partial tiles (from a global workspace) in slice order.
+// SMs, each is split over K in two.  Where every unit gets its own CTA, the two
+// slices of a tile run as the two CTAs of a cluster: each finishes half of the
+// tile's tokens, taking the other slice's partial sums for that half from its
+// peer through distributed shared memory.  Otherwise the slice that arrives last
+// adds both partial tiles from a global workspace in slice order.
 // Every mbarrier wait is bounded; a wait that gives up records an error code
 // in the device status word, raises a CTA-wide abort flag and lets every role
 // leave its loop; TMEM is always released before exit.
+#include <cooperative_groups.h>
 #include <cuda.h>
 
 #include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
 
 #include "il_internal.cuh"
 #include "il_ptx.cuh"
@@ -75,6 +81,8 @@ struct GemmParams {  // CUtensorMap members give it their 64-byte (or larger) al
   int stall_producer;  // failure-detection test: the producer never loads, so the MMA wait runs out
   unsigned* status;
   unsigned glu_mask;   // bit j: job j's rows interleave gate/up; y[j] is h = gelu(g) * u, n_out/2 wide
+  int pair;            // split-K in two, one unit per CTA, the two slices of a tile the two CTAs of a
+                       // cluster: partial sums exchanged through distributed shared memory (no ws)
 };
 static_assert(alignof(GemmParams) >= 64, "tensor maps must stay 64-byte aligned in the kernel parameters");
 static_assert(sizeof(GemmParams) <= 4096, "kernel parameters must fit the classic 4 KB limit");
@@ -292,6 +300,9 @@ __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid
   const uint32_t tmem_base = *tmem_slot;
   // set-up above overlaps the previous kernel; x (bf16 copy) and y need it finished
   grid_dep_wait();
+  // split-K pair: the tile whose accumulator (buffer 0) this CTA's epilogue holds
+  bool pair_ready = false;
+  int pair_job = 0, pair_mt = 0, pair_nt = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -451,6 +462,13 @@ __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid
       tc_fence_after();
       int job, mt, nt;
       locate_tile(p, tile, job, mt, nt);
+      if (p.pair) {  // the CTA's only unit: finished below, with the peer
+        pair_ready = true;
+        pair_job = job;
+        pair_mt = mt;
+        pair_nt = nt;
+        break;
+      }
       const int n_out = p.n_out[job];
       float* y = p.y[job];
       const bool glu = (p.glu_mask >> job) & 1u;  // uniform over the CTA
@@ -546,6 +564,79 @@ __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid
               for (int j = 0; j < kFix; ++j)
                 if (c0 + j < ntok) y[(int64_t)(nt * BN + c0 + j) * n_out + row] = v[j];
             }
+          }
+        }
+      }
+    }
+  }
+
+  if (p.pair) {
+    // ---- split-K pair.  Every thread of both CTAs takes part in the two cluster
+    // barriers (after a wait that gave up too, so the peer never waits for ever).
+    // Rank r finishes tokens [r * BN/2, (r + 1) * BN/2) of the tile: it receives the
+    // other slice's partial sums of those tokens into its (now idle) pipeline memory,
+    // [BN/2 tokens][kBM rows] fp32, and sends its own partial sums of the peer's half.
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    float* xbuf = reinterpret_cast<float*>(tiles);
+    const int quarter = warp & 3;
+    const int lrow = quarter * 32 + lane;
+    const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);  // accumulator buffer 0
+    // (1) both CTAs' MMAs are complete and every load consumed: the pipeline memory is free
+    __syncwarp();
+    tc_fence_before();
+    cluster.sync();
+    tc_fence_after();
+    // uniform over the warp (the abort flag is read once per lane)
+    const bool live = __all_sync(0xffffffffu, warp >= 2 && warp < 6 && pair_ready && !*abort_flag);
+    if (live) {
+      float* peer = cluster.map_shared_rank(xbuf, rank ^ 1);
+      const int c_peer = (rank ^ 1) * (BN / 2);
+#pragma unroll 1
+      for (int c = 0; c < BN / 2; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c_peer + c, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) peer[(c + j) * kBM + lrow] = __uint_as_float(r[j]);
+      }
+    }
+    // (2) the peer's partial sums of this CTA's half have landed
+    __syncwarp();
+    tc_fence_before();
+    cluster.sync();
+    tc_fence_after();
+    if (live) {
+      const int n_out = p.n_out[pair_job];
+      float* y = p.y[pair_job];
+      const bool glu = (p.glu_mask >> pair_job) & 1u;
+      const int row = pair_mt * kBM + lrow;
+      const int c_own = rank * (BN / 2);
+#pragma unroll 1
+      for (int c = 0; c < BN / 2; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c_own + c, r);
+        // slice 0 + slice 1 (two operands: the same sum on either rank)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + xbuf[(c + j) * kBM + lrow]);
+        const int tok0 = pair_nt * BN + c_own + c;
+        if (glu) {
+          // as in the direct store: lanes 2i / 2i+1 (gate / up) trade halves of the 32 tokens
+          const bool odd = lane & 1;
+          const int tk0 = tok0 + (odd ? 16 : 0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float keep = __uint_as_float(odd ? r[j + 16] : r[j]);
+            const float got = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? r[j] : r[j + 16]), 1);
+            const int tok = tk0 + j;
+            if (row < n_out && tok < p.t)
+              y[(int64_t)tok * (n_out >> 1) + (row >> 1)] = odd ? gelu_mul(got, keep) : gelu_mul(keep, got);
+          }
+        } else if (row < n_out) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int tok = tok0 + j;
+            if (tok < p.t) y[(int64_t)tok * n_out + row] = __uint_as_float(r[j]);
           }
         }
       }
@@ -779,6 +870,35 @@ bool make_scale_map(CUtensorMap* m, const PackedWeight& w) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Clusters of two CTAs of gemm_kernel<BN, FMT> that fit on the device at once
+// (once per device; 0 if the query fails).
+template <int BN, int FMT>
+int pair_clusters(int dev, size_t smem) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeClusterDimension;
+  a.val.clusterDim.x = 2;
+  a.val.clusterDim.y = 1;
+  a.val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(gemm_threads(FMT));
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = &a;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, FMT>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[dev] = n;
+  return n;
+}
+
 template <int FMT>
 cudaError_t prepare_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pad, const GemmJob* jobs, int n_jobs,
                              int num_sms, unsigned* status, void* ws, size_t ws_bytes, std::vector<Launch>* out) {
@@ -798,7 +918,9 @@ cudaError_t prepare_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
     const int nj = n_jobs - j0 < kMaxGemmJobs ? n_jobs - j0 : kMaxGemmJobs;
     Plan pl = plan_launch(t, n_in_pad, jobs + j0, nj, num_sms, ws != nullptr);
     const size_t cbytes = kCounterBytes;
-    if (pl.splits > 1 &&
+    // a split in two whose units all fit at once as CTA pairs needs no workspace
+    const bool pair = pl.splits == 2 && pl.total_tiles <= pair_clusters<BN, FMT>(dev, smem);
+    if (!pair && pl.splits > 1 &&
         cbytes + (size_t)pl.total_tiles * pl.splits * BN * kBM * sizeof(float) > ws_bytes) {
       pl.splits = 1;
       pl.kb_per_split = (int)(n_in_pad / kBK);
@@ -812,7 +934,8 @@ cudaError_t prepare_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
     p.splits = pl.splits;
     p.kb_per_split = pl.kb_per_split;
     p.status = status;
-    if (pl.splits > 1) {
+    p.pair = pair ? 1 : 0;
+    if (pl.splits > 1 && !pair) {
       // counters are zero when the workspace is created and the last arriver of
       // every tile puts its counter back to zero (see kCounterBytes)
       p.counters = static_cast<unsigned*>(ws);
@@ -845,9 +968,11 @@ cudaError_t prepare_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
     const int units = tiles * p.splits;
     Launch L;
     L.fn = reinterpret_cast<const void*>(gemm_kernel<BN, FMT>);
-    L.grid = dim3(units < num_sms ? units : num_sms);
+    // pair: one CTA per unit, a tile's two slices in one cluster (units 2i, 2i + 1)
+    L.grid = dim3(pair ? units : (units < num_sms ? units : num_sms));
     L.block = dim3(gemm_threads(FMT));
     L.smem = smem;
+    if (pair) L.set_cluster(2);
     if (kUsePdl) L.allow_early_start();
     if (!L.set_args(p)) return cudaErrorMemoryAllocation;
     out->push_back(L);
