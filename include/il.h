@@ -306,8 +306,9 @@ int il_last_status(void);
 
 /* Copies the cumulative counters into *out (the page's `Backend::stats`, a
  * cumulative timing summary when profiling).  With IL_PROFILE=1 in the
- * environment, il_matmul_batch and il_centroid_head record a CUDA event before
- * and after their launches on their stream (not while the stream is being
+ * environment, il_matmul_batch, il_matmul_batch_host (its launches, not its
+ * copies) and il_centroid_head record a CUDA event before and after their
+ * launches on their stream (not while the stream is being
  * captured, and not il_matmul_batch_noalloc); il_get_stats then waits for every
  * recorded call to finish and adds its device time to device_ns.  Without
  * IL_PROFILE nothing is recorded and nothing waits.  The entry points also mark
