@@ -165,7 +165,8 @@ int il_matmul_batch_host(const float* x, int64_t t, int64_t n_in, const il_job* 
  * il_matmul_batch_noalloc -- the pages have no counterpart of this entry point.
  * Same arguments and checks as il_matmul_batch, the same split over the decode
  * and tensor-core kernels, results equal to il_matmul_batch's within the
- * per-element tolerance (the tensor-core launches here never split K), and
+ * per-element tolerance (the tensor-core launches here split K only where the
+ * two slices of a tile can run as a CTA pair, which needs no workspace), and
  * the same rule that an error enqueues nothing -- but it never allocates
  * device memory: for callers that cannot let a library call cudaMalloc, such
  * as services that give all device memory to their own pool at start-up, or

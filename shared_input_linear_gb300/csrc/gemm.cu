@@ -916,7 +916,8 @@ cudaError_t prepare_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
   }
   for (int j0 = 0; j0 < n_jobs; j0 += kMaxGemmJobs) {
     const int nj = n_jobs - j0 < kMaxGemmJobs ? n_jobs - j0 : kMaxGemmJobs;
-    Plan pl = plan_launch(t, n_in_pad, jobs + j0, nj, num_sms, ws != nullptr);
+    // without a workspace a split survives only in the CTA-pair form below
+    Plan pl = plan_launch(t, n_in_pad, jobs + j0, nj, num_sms, true);
     const size_t cbytes = kCounterBytes;
     // a split in two whose units all fit at once as CTA pairs needs no workspace
     const bool pair = pl.splits == 2 && pl.total_tiles <= pair_clusters<BN, FMT>(dev, smem);

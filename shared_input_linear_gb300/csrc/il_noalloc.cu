@@ -118,7 +118,7 @@ extern "C" int il_matmul_batch_noalloc(const float* x, int64_t t, int64_t n_in, 
   if (t == 0 || n_jobs == 0) return IL_OK;
 
   // the same split over the kernels as il_matmul_batch; x's bf16 copy goes to the
-  // static scratch and the tensor-core launches never split K (no workspace)
+  // static scratch and the tensor-core launches split K only as CTA pairs (no workspace)
   BatchPlan plan;
   plan_batch(t, jobs, n_jobs, ws, /*gemm_quant=*/true, &plan);
   if (plan.xb_bytes > kNoAllocScratchBytes)
@@ -128,7 +128,7 @@ extern "C" int il_matmul_batch_noalloc(const float* x, int64_t t, int64_t n_in, 
   rc = setup_device(dev, stream, &slot);
   if (rc != IL_OK) return rc;
   std::vector<Launch> launches;
-  // the tensor-core launches see no workspace (they never split K here); the
+  // the tensor-core launches see no workspace (a split runs as CTA pairs or not at all); the
   // decode launches get the static one
   BatchPlan gplan = plan, dplan = plan;
   for (int f = 0; f < 3; ++f) gplan.decode[f].clear();
