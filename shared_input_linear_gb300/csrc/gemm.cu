@@ -919,8 +919,12 @@ cudaError_t prepare_gemm_fmt(const __nv_bfloat16* xb, int64_t t, int64_t n_in_pa
     // without a workspace a split survives only in the CTA-pair form below
     Plan pl = plan_launch(t, n_in_pad, jobs + j0, nj, num_sms, true);
     const size_t cbytes = kCounterBytes;
-    // a split in two whose units all fit at once as CTA pairs needs no workspace
-    const bool pair = pl.splits == 2 && pl.total_tiles <= pair_clusters<BN, FMT>(dev, smem);
+    // a split in two whose units all fit at once as CTA pairs needs no workspace.
+    // IL_TEST_SPLIT_WORKSPACE=1 (tests only) sends every split through the global
+    // workspace, the path taken when the pairs do not fit, so that it stays covered.
+    const char* force_ws = getenv("IL_TEST_SPLIT_WORKSPACE");
+    const bool pair = !(force_ws != nullptr && force_ws[0] == '1') && pl.splits == 2 &&
+                      pl.total_tiles <= pair_clusters<BN, FMT>(dev, smem);
     if (!pair && pl.splits > 1 &&
         cbytes + (size_t)pl.total_tiles * pl.splits * BN * kBM * sizeof(float) > ws_bytes) {
       pl.splits = 1;

@@ -239,12 +239,14 @@ import shared_input_linear_gb300 as sil
 import workloads as wl
 import oracle
 fmt, t, entry = {fmt!r}, {t!r}, {entry!r}
+if entry == "batch_ws":                  # split K through the global workspace, not CTA pairs
+    os.environ["IL_TEST_SPLIT_WORKSPACE"] = "1"
 b = wl.make_batch(512, (96, 40), t, fmt, seed=4)
 ws = [sil.upload_weight(f, buf, n, 512) for f, buf, n in b.jobs]
 x = torch.from_numpy(b.x).cuda()
 ys = [torch.zeros(t, n, device="cuda") for _, _, n in b.jobs]
 jobs = [(w, n, y.data_ptr()) for w, (_, _, n), y in zip(ws, b.jobs, ys)]
-call = sil.matmul_batch_ptr if entry == "batch" else sil.matmul_batch_noalloc_ptr
+call = sil.matmul_batch_noalloc_ptr if entry == "noalloc" else sil.matmul_batch_ptr
 s = torch.cuda.current_stream().cuda_stream
 call(x.data_ptr(), t, 512, jobs, s)      # a warm call: the entry point is set up
 torch.cuda.synchronize()
@@ -273,6 +275,8 @@ print("AFTER", ok)
     ("q4", 1, "batch"),      # Q8/Q4 decode kernel: its bulk-copy waits
     ("q8", 6, "batch"),
     ("bf16", 16, "noalloc"),  # tensor-core kernel through the no-alloc entry point
+    ("bf16", 24, "batch"),    # tensor-core kernel, split K as CTA pairs (cluster barriers)
+    ("q8", 24, "batch_ws"),   # tensor-core kernel, split K through the global workspace
     ("q4", 3, "noalloc"),     # decode kernel through the no-alloc entry point
 ])
 def test_stalled_copies_report_timeout(fmt, t, entry):

@@ -464,3 +464,21 @@ def test_largest_n_in(sil, fmt, t):
     ys, guards = run(sil, b)
     assert guards
     assert_parity(b, ys, "n_in 32768")
+
+
+def test_split_k_pair_and_workspace_forms(sil, monkeypatch):
+    # tile counts that split K in two: as CTA pairs exchanging partial sums through
+    # distributed shared memory, then (IL_TEST_SPLIT_WORKSPACE=1) through the global
+    # workspace, the form taken when the pairs do not fit; both against the oracle,
+    # and bitwise equal (both add the same two slices)
+    outs = {}
+    for form in ("0", "1"):
+        monkeypatch.setenv("IL_TEST_SPLIT_WORKSPACE", form)
+        for fmt, t, n_in, n_out in (("bf16", 40, 1024, 1000), ("q8", 300, 2048, 520), ("q4", 512, 12288, 4096)):
+            b = wl.make_batch(n_in, (n_out,), t, fmt, seed=n_out + t)
+            ys, guards = run(sil, b)
+            assert guards
+            assert_parity_sampled(b, ys, n_samples=128, what=f"{fmt} t={t} form={form}")
+            outs.setdefault((fmt, t), []).append(ys[0])
+    for k, v in outs.items():
+        assert np.array_equal(v[0].view(np.uint32), v[1].view(np.uint32)), k
