@@ -242,6 +242,27 @@ __device__ __forceinline__ uint4 dequant_unit(const uint32_t* __restrict__ qw, c
                     f2bf16x2(f2mul(dd, qp[3])));
 }
 
+// Gate/up epilogue of 32 token columns held by a lane pair: lanes 2i (gate row) and
+// 2i+1 (up row) of output column i each finish 16 of the tokens, trading the other
+// half with the partner (the even lane keeps r[0..15], the odd lane r[16..31]; tok0 is
+// the lane's first token).  All 16 activations are computed before any store, so
+// their latency chains overlap.  h: this column of the output (stride h_ld per
+// token); store: the column lies inside the weight.
+__device__ __forceinline__ void glu_store16(const uint32_t (&r)[32], bool odd, bool store, int tok0, int t,
+                                            float* h, int h_ld) {
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float keep = __uint_as_float(odd ? r[j + 16] : r[j]);
+    const float got = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? r[j] : r[j + 16]), 1);
+    v[j] = gelu_mul(odd ? got : keep, odd ? keep : got);
+  }
+  if (!store) return;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (tok0 + j < t) h[(int64_t)(tok0 + j) * h_ld] = v[j];
+}
+
 template <int BN, int FMT>
 __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   constexpr bool kQ = FMT != IL_BF16;
@@ -490,15 +511,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid
           // trading the other half with its partner.  n_out is even, so a pair is
           // either wholly inside or wholly outside the weight.
           const bool odd = lane & 1;
-          const int tok0 = nt * BN + c0 + (odd ? 16 : 0);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float keep = __uint_as_float(odd ? r[j + 16] : r[j]);
-            const float got = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? r[j] : r[j + 16]), 1);
-            const int tok = tok0 + j;
-            if (row < n_out && tok < p.t)
-              y[(int64_t)tok * (n_out >> 1) + (row >> 1)] = odd ? gelu_mul(got, keep) : gelu_mul(keep, got);
-          }
+          glu_store16(r, odd, row < n_out, nt * BN + c0 + (odd ? 16 : 0), p.t, y + (row >> 1), n_out >> 1);
         } else {
           const int tok0 = nt * BN + c0;
           if (row < n_out) {
@@ -551,13 +564,17 @@ __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid
             if (glu) {
               // as in the direct store: the even lane finishes the first half, the odd the second
               const bool odd = lane & 1;
+              float h[kFix / 2];
 #pragma unroll
-              for (int j = 0; j < kFix / 2; ++j) {
+              for (int j = 0; j < kFix / 2; ++j) {  // every activation first: independent chains
                 const float keep = odd ? v[j + kFix / 2] : v[j];
                 const float got = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + kFix / 2], 1);
+                h[j] = gelu_mul(odd ? got : keep, odd ? keep : got);
+              }
+#pragma unroll
+              for (int j = 0; j < kFix / 2; ++j) {
                 const int c = c0 + j + (odd ? kFix / 2 : 0);
-                if (row < n_out && c < ntok)
-                  y[(int64_t)(nt * BN + c) * (n_out >> 1) + (row >> 1)] = odd ? gelu_mul(got, keep) : gelu_mul(keep, got);
+                if (row < n_out && c < ntok) y[(int64_t)(nt * BN + c) * (n_out >> 1) + (row >> 1)] = h[j];
               }
             } else {
 #pragma unroll
@@ -623,15 +640,7 @@ __global__ void __launch_bounds__(gemm_threads(FMT), 1) gemm_kernel(const __grid
         if (glu) {
           // as in the direct store: lanes 2i / 2i+1 (gate / up) trade halves of the 32 tokens
           const bool odd = lane & 1;
-          const int tk0 = tok0 + (odd ? 16 : 0);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float keep = __uint_as_float(odd ? r[j + 16] : r[j]);
-            const float got = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? r[j] : r[j + 16]), 1);
-            const int tok = tk0 + j;
-            if (row < n_out && tok < p.t)
-              y[(int64_t)tok * (n_out >> 1) + (row >> 1)] = odd ? gelu_mul(got, keep) : gelu_mul(keep, got);
-          }
+          glu_store16(r, odd, row < n_out, tok0 + (odd ? 16 : 0), p.t, y + (row >> 1), n_out >> 1);
         } else if (row < n_out) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
