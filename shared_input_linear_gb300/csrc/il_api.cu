@@ -971,6 +971,7 @@ size_t plan_workspace_bytes(const BatchPlan& plan, int64_t t, int64_t n_in, cons
     if (!plan.gemm[f].empty())
       need = std::max(need, gemm_workspace_bytes(t, plan.n_in_pad, plan.gemm[f].data(), (int)plan.gemm[f].size(),
                                                  num_sms));
+  if (plan.decode[IL_Q8].empty() && plan.decode[IL_Q4].empty()) return need;  // only Q8/Q4 decode splits
   std::vector<std::pair<int, DecodeParams>> dl;
   decode_launch_params(plan, nullptr, t, n_in, jobs, ws, &dl);
   for (const auto& fp : dl)

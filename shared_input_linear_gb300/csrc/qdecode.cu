@@ -676,6 +676,24 @@ bool plan_q(int fmt, int t, int n_chunks, int total_tiles, int num_sms, int smem
   return best > 0.0;
 }
 
+// plan_q is a pure function of its arguments (t only through its instance TT); a
+// call of a shape seen before on this thread reuses the plan.
+bool plan_q_memo(int fmt, int t, int n_chunks, int total_tiles, int num_sms, int smem_limit, size_t ws_room,
+                 QPlan* out) {
+  using Key = std::tuple<int, int, int, int, int, int, size_t>;
+  thread_local std::map<Key, std::pair<bool, QPlan>> memo;
+  const Key key{fmt, q_tt(t), n_chunks, total_tiles, num_sms, smem_limit, ws_room};
+  auto it = memo.find(key);
+  if (it == memo.end()) {
+    if (memo.size() >= 512) memo.clear();
+    QPlan pl;
+    const bool ok = plan_q(fmt, t, n_chunks, total_tiles, num_sms, smem_limit, ws_room, &pl);
+    it = memo.emplace(key, std::make_pair(ok, pl)).first;
+  }
+  *out = it->second.second;
+  return it->second.first;
+}
+
 }  // namespace
 
 size_t qdecode_workspace_bytes(int fmt, const DecodeParams& d, int num_sms) {
@@ -683,7 +701,7 @@ size_t qdecode_workspace_bytes(int fmt, const DecodeParams& d, int num_sms) {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   const int limit = q_smem_limit(dev);
   QPlan pl;
-  if (limit <= 0 || !plan_q(fmt, d.t, d.n_chunks, d.total_groups / 2, num_sms, limit, SIZE_MAX, &pl)) return 0;
+  if (limit <= 0 || !plan_q_memo(fmt, d.t, d.n_chunks, d.total_groups / 2, num_sms, limit, SIZE_MAX, &pl)) return 0;
   return pl.ws_bytes;
 }
 
@@ -698,7 +716,7 @@ cudaError_t prepare_qdecode(int fmt, const DecodeParams& d, int num_sms, unsigne
   const int limit = q_smem_limit(dev);
   if (limit <= 0) return cudaErrorInvalidValue;
   QPlan pl;
-  if (!plan_q(fmt, d.t, d.n_chunks, d.total_groups / 2, num_sms, limit, ws != nullptr ? ws_bytes : 0, &pl))
+  if (!plan_q_memo(fmt, d.t, d.n_chunks, d.total_groups / 2, num_sms, limit, ws != nullptr ? ws_bytes : 0, &pl))
     return cudaErrorInvalidValue;
 
   QParams p;
