@@ -110,9 +110,10 @@ def test_tensor_core_long_k(sil, fmt, t, n_in, n_outs):
     assert_parity(b, ys, "long K")
 
 
-def test_stream_k_growing_tile_counts(sil):
-    # consecutive tensor-core batches on one stream whose tile counts grow: the
-    # per-tile arrival counters of the split tiles must start at zero every time
+def test_split_k_growing_tile_counts(sil):
+    # consecutive tensor-core batches on one stream whose tile counts grow (split K as
+    # CTA pairs at the few-tile ones): the per-tile arrival counters of split tiles
+    # must start at zero every time (IL_TEST_SPLIT_WORKSPACE covers that form)
     import torch
     s = torch.cuda.Stream()
     for fmt, t, n_in, n_out in (("bf16", 300, 4096, 128), ("q4", 600, 4096, 1024), ("bf16", 1000, 4096, 4096),
