@@ -505,11 +505,15 @@ __global__ void __launch_bounds__(kQThreads, 1) qdecode_kernel(const __grid_cons
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
       const int e = lane + 32 * i;
-      float s = 0.f;
+      if (p.wk == 1) {  // the warp's own partial (uniform over the grid)
+        v[i] = pr[e];
+      } else {
+        float s = 0.f;
 #pragma unroll
-      for (int k = 0; k < kQWarps; ++k)
-        if (k < p.wk) s += pr[(size_t)k * TT * 16 + e];
-      v[i] = s;
+        for (int k = 0; k < kQWarps; ++k)
+          if (k < p.wk) s += pr[(size_t)k * TT * 16 + e];
+        v[i] = s;
+      }
     }
     __syncwarp();
     if (lane == 0) {
