@@ -220,3 +220,26 @@ def test_mixed_formats_and_fused_gate_up_on_host_buffers(t, pinned):
         fused.free()
         for w in pw:
             w.free()
+
+
+@pytest.mark.parametrize("x_pinned,y_pinned", [(True, False), (False, True)])
+def test_pinned_and_pageable_buffers_mixed(x_pinned, y_pinned):
+    # x used in place and y copied back, or x copied in and y written in place
+    import torch
+    sil = lib()
+    for fmt, t in (("bf16", 3), ("q4", 40)):
+        b = wl.make_batch(384, (136, 64), t, fmt, seed=t + 77)
+        ws = upload(sil, b)
+        try:
+            x = torch.from_numpy(b.x)
+            x = x.pin_memory() if x_pinned else x.clone()
+            bufs = [torch.full((2 * GUARD + t * n,), float("nan"), pin_memory=y_pinned) for _, _, n in b.jobs]
+            ys = [buf[GUARD:GUARD + t * n].view(t, n) for buf, (_, _, n) in zip(bufs, b.jobs)]
+            sil.matmul_batch_host(x, list(zip(ws, ys)))
+            for buf, (_, _, n) in zip(bufs, b.jobs):
+                h = buf.numpy()
+                assert np.all(np.isnan(np.concatenate([h[:GUARD], h[GUARD + t * n:]])))
+            assert_parity(b, [y.numpy().copy() for y in ys], what=f"{fmt} x_pinned={x_pinned}")
+        finally:
+            for w in ws:
+                w.free()
